@@ -1,0 +1,123 @@
+// quant.cuh -- shared-memory operand layouts and the NVFP4 activation
+// quantiser run on the GPU.
+//
+// Operand layouts (tcgen05, K-major, 128-byte swizzle): a K-block is 128 bytes
+// of every row (64 bf16 or 256 fp4 elements); rows are 128 B apart and 8-row
+// groups 1024 B apart; the 16-byte chunk c of row r sits at chunk c ^ (r % 8).
+//
+// Scale-factor layout (block-scaled MMA, one E4M3 per 16 elements): a chunk
+// covers 128 rows x 64 elements (4 scale bytes per row) in 512 bytes; the
+// scale of row m, sub-block j (0..3) is byte (m % 32) * 16 + (m / 32) * 4 + j.
+//
+// Quantiser (the expert inputs: one row = one token's pooled vector, or one
+// (token, expert) pair's SwiGLU output), page "Muse Spark Open: 1,109 Tokens a
+// Second Is a Kernel Change, Not a Model Change", section "Where the kernel
+// boundary sits ...": the expert GEMMs consume fp4 activations.  Each step is
+// a correctly rounded float32 operation:
+//   s_row = amax(|row|) / 2688  (1 when the row is all zero)
+//   per 16 elements: s_b = E4M3_rn_satfinite(amax16 / (6 * s_row)),
+//                    q_i = E2M1_rn_satfinite(x_i / (s_b * s_row)), 0 if s_b = 0.
+#pragma once
+#include "ptx.cuh"
+
+namespace mk {
+
+// Byte offset of (row r, byte b of the row's K-block) inside one K-block tile
+// of an operand with 128-byte swizzle.
+MK_DEV uint32_t sw128_offset(uint32_t r, uint32_t b) {
+  return (r >> 3) * 1024u + (r & 7u) * 128u + ((((b >> 4) ^ r) & 7u) << 4) + (b & 15u);
+}
+
+MK_DEV uint32_t sf_atom_offset(uint32_t m, uint32_t j) {
+  return (m & 31u) * 16u + (m >> 5) * 4u + j;
+}
+
+MK_DEV float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+MK_DEV float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+MK_DEV void load_bf16x16(const __nv_bfloat16* p, float (&x)[16]) {
+  const uint4* q = reinterpret_cast<const uint4*>(p);
+  uint4 a = q[0], b = q[1];
+  uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// One warp quantises one row of K bf16 values (K % 16 == 0, row 16-byte
+// aligned).  For every 16-element block b the sink receives the 8 code bytes
+// (two 32-bit words, element 16b in the low nibble of the first byte) and the
+// scale byte.  Returns s_row (same value in every lane).
+template <class Sink>
+MK_DEV float quantize_row_nvfp4(const __nv_bfloat16* row, int K, Sink& sink) {
+  const int lane = lane_id();
+  const int nblk = K >> 4;
+  float amax = 0.f;
+  for (int b = lane; b < nblk; b += 32) {
+    float x[16];
+    load_bf16x16(row + b * 16, x);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  }
+  amax = warp_max(amax);
+  const float s_row = amax > 0.f ? __fdiv_rn(amax, 2688.0f) : 1.0f;
+  const float d6 = __fmul_rn(6.0f, s_row);
+  for (int b = lane; b < nblk; b += 32) {
+    float x[16];
+    load_bf16x16(row + b * 16, x);
+    float a16 = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) a16 = fmaxf(a16, fabsf(x[i]));
+    const uint32_t sb = cvt_e4m3(__fdiv_rn(a16, d6));
+    const float sbf = e4m3_to_float(sb);
+    uint32_t w0 = 0, w1 = 0;
+    if (sbf > 0.f) {
+      const float c = __fmul_rn(sbf, s_row);
+      float r[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) r[i] = __fdiv_rn(x[i], c);
+      w0 = cvt_e2m1x4(r[0], r[1], r[2], r[3]) | (cvt_e2m1x4(r[4], r[5], r[6], r[7]) << 16);
+      w1 = cvt_e2m1x4(r[8], r[9], r[10], r[11]) | (cvt_e2m1x4(r[12], r[13], r[14], r[15]) << 16);
+    }
+    sink.put(b, w0, w1, sb);
+  }
+  return s_row;
+}
+
+// Sink writing row-major codes [K/2] and scales [K/16] (used by self-tests).
+struct RowMajorSink {
+  uint8_t* codes;
+  uint8_t* scales;
+  MK_DEV void put(int b, uint32_t w0, uint32_t w1, uint32_t sb) {
+    reinterpret_cast<uint2*>(codes)[b] = make_uint2(w0, w1);
+    scales[b] = static_cast<uint8_t>(sb);
+  }
+};
+
+// Sink writing row `r` of a block-scaled MMA operand: codes into K-blocks of
+// 2048 bytes (16 rows x 128 B, 128-byte swizzle) and scales into 512-byte
+// chunks (one per 64 elements).
+struct OperandSink {
+  uint8_t* codes;   // K-block 0 of the operand
+  uint8_t* sf;      // chunk 0 of the scale factors
+  uint32_t r;       // operand row (< 16)
+  MK_DEV void put(int b, uint32_t w0, uint32_t w1, uint32_t sb) {
+    const uint32_t byte = static_cast<uint32_t>(b) * 8u;          // byte in row
+    const uint32_t kb = byte >> 7;
+    *reinterpret_cast<uint2*>(codes + kb * 2048u + sw128_offset(r, byte & 127u)) =
+        make_uint2(w0, w1);
+    sf[(b >> 2) * 512u + sf_atom_offset(r, b & 3)] = static_cast<uint8_t>(sb);
+  }
+};
+
+}  // namespace mk
