@@ -1,0 +1,107 @@
+// layer.h -- parameters of the persistent decode-layer kernel, shared by the
+// host launcher (api.cu) and the kernel (layer.cu).
+#pragma once
+#include <cuda.h>
+#include <cstdint>
+
+namespace mk {
+
+constexpr int kThreads = 256;     // 8 warps: TMA, MMA, 2 stagers, 4 epilogue/math
+constexpr int kStages = 7;        // weight ring depth (16 KB tile + 2 KB scales)
+constexpr int kKC = 512;          // K elements per split-K unit (bf16 phases)
+constexpr int kMaxT = 16;         // verify tokens per step (MMA N)
+constexpr int kMaxE = 256;
+constexpr int kMaxK = 8;          // top-k
+constexpr int kTmemCols = 256;
+constexpr int kNumCounters = 8;   // grid-wide dependency counters
+
+// Phases of one launch, in order.
+enum PhaseId : int {
+  PH_QKV = 0,      // first layer: RMSNorm(x_in) -> QKV, K/V rows written
+  PH_ATTN = 1,     // split-KV GQA attention partials
+  PH_MERGE = 2,    // merge of the attention partials -> o
+  PH_O = 3,        // o-proj + residual -> x_mid
+  PH_RP = 4,       // router (+ top-k) and pooler (MoE) | dense gate/up
+  PH_GU = 5,       // expert gate/up (MoE)
+  PH_DOWN = 6,     // expert down + combine (MoE) | dense down + residual
+  PH_UNPOOL = 7,   // unpooler + residual (MoE)
+  PH_NQKV = 8,     // fused next-layer RMSNorm -> QKV, next K/V rows written
+  PH_COUNT = 9
+};
+
+// Grid dependency counters (one per dependency stop).
+enum BarrierId : int {
+  BAR_QKV = 0, BAR_ATTN = 1, BAR_MERGE = 2, BAR_O = 3, BAR_RP = 4, BAR_GU = 5, BAR_DOWN = 6,
+  BAR_LAST = 7
+};
+
+struct LayerParams {
+  // tensor maps (weights; 128-row x 128-byte boxes, 128-byte swizzle)
+  CUtensorMap tm_qkv, tm_o, tm_router, tm_pool, tm_unpool, tm_nqkv, tm_gate, tm_up, tm_down;
+
+  // shapes
+  int H, Hq, Hkv, d, window, E, topk, P, I, F, moe, first_layer, fuse_next, renorm;
+  int Nqkv;                 // Hq*d + 2*Hkv*d
+  float eps;
+  uint64_t timeout_ns;
+  int grid;
+
+  // per-step
+  int T, ctx;
+  const __nv_bfloat16* x_in;
+  __nv_bfloat16* x_out;
+  const __nv_bfloat16* q_in;      // !first_layer
+  __nv_bfloat16* k_cache;
+  __nv_bfloat16* v_cache;
+  __nv_bfloat16* nk_cache;
+  __nv_bfloat16* nv_cache;
+  __nv_bfloat16* q_out;
+  int32_t* topk_idx_out;
+  float* topk_w_out;
+
+  // weights used outside TMA
+  const __nv_bfloat16* attn_norm_w;
+  const __nv_bfloat16* ffn_norm_w;
+  const __nv_bfloat16* next_attn_norm_w;
+  const float* ts_gate;
+  const float* ts_up;
+  const float* ts_down;
+  const uint8_t* sf_gate;   // repacked scale factors (library-owned)
+  const uint8_t* sf_up;
+  const uint8_t* sf_down;
+
+  // attention split
+  int attn_chunks;          // chunks per KV head
+  int attn_chunk_len;       // positions per chunk (multiple of 64)
+  int attn_lo;              // first key position any verify token sees
+
+  // split-K geometry of the bf16 phases: tiles of 128 rows x ksplit
+  int ks_qkv, ks_o, ks_rp, ks_dgu, ks_ddown, ks_unpool;
+  int tiles_qkv, tiles_o, tiles_router, tiles_pool, tiles_dgu, tiles_ddown, tiles_unpool;
+
+  // library-owned scratch
+  __nv_bfloat16* q_buf;     // [16][Hq*d]  (first layer)
+  __nv_bfloat16* o_buf;     // [16][Hq*d]
+  __nv_bfloat16* xmid;      // [16][H]
+  __nv_bfloat16* p_buf;     // [16][P]
+  __nv_bfloat16* a_buf;     // MoE [16*k][I]; dense [16][F]
+  __nv_bfloat16* z_buf;     // [16*k][P]
+  __nv_bfloat16* y_buf;     // [16][P]
+  float* logits;            // [16][E]
+  int32_t* idx;             // [16][k]
+  float* wts;               // [16][k]
+  float* ssq_mid;           // [H/128][16]
+  float* ssq_out;           // [H/128][16]
+  float* pamax;             // [P/128][16]
+  float* aamax;             // [16*k][I/128]
+  float* part;              // split-K partials (sized for the largest phase)
+  float* attn_part;         // [Hkv*chunks][64][d + 2]
+  uint32_t* fix_ctr;        // fixup counters per (phase, tile)  [PH_COUNT][256]
+  uint32_t* comb_ctr;       // combine counters [16][P/128]
+  uint32_t* misc_ctr;       // [0]: router tiles done
+  uint32_t* bar_ctr;        // [kNumCounters] grid dependency counters
+  uint32_t* epoch;          // launches of this layer so far
+  uint32_t* status;         // sticky error word
+};
+
+}  // namespace mk
