@@ -28,6 +28,16 @@ mk_status mk_selftest_quantize(const void* x, int32_t rows, int32_t K, void* cod
 mk_status mk_selftest_mma(int32_t fp4, const void* a, const void* a_scales, const void* b,
                           const void* b_scales, int32_t K, float* out, void* stream);
 
+/* Copy `bytes` of a layer's library-owned intermediate buffer to the device
+ * buffer `dst` (synchronous; call after the step's stream has synchronised).
+ * which: 0 q [16, Hq*d] bf16 (first layer), 1 o [16, Hq*d] bf16,
+ *        2 x_mid [16, H] bf16, 3 logits [16, 256] f32, 4 p [16, P] bf16,
+ *        5 a [16*k, I] bf16 (dense: [16, F]), 6 z [16*k, P] bf16,
+ *        7 y [16, P] bf16, 8 idx [16, k] int32, 9 w [16, k] f32.
+ * MK_ERR_INVALID_ARG if the buffer does not exist for this layer or `bytes`
+ * exceeds it. */
+mk_status mk_selftest_copy_scratch(mk_layer* layer, int32_t which, void* dst, size_t bytes);
+
 #ifdef __cplusplus
 }
 #endif

@@ -100,10 +100,13 @@ _lib_mk_selftest_quantize = _sig("mk_selftest_quantize", _c.c_int,
 _lib_mk_selftest_mma = _sig("mk_selftest_mma", _c.c_int,
                             [_c.c_int32, _vp, _vp, _vp, _vp, _c.c_int32, _vp, _vp])
 
+_lib_mk_selftest_copy_scratch = _sig("mk_selftest_copy_scratch", _c.c_int,
+                                     [_vp, _c.c_int32, _vp, _c.c_size_t])
+
 EXPORTED = ["mk_layer_create", "mk_decode_step", "mk_layer_status", "mk_layer_clear_status",
             "mk_layer_destroy", "mk_stack_create", "mk_stack_step", "mk_stack_status",
             "mk_stack_destroy", "mk_status_string", "mk_layer_get_info",
-            "mk_selftest_quantize", "mk_selftest_mma"]
+            "mk_selftest_quantize", "mk_selftest_mma", "mk_selftest_copy_scratch"]
 
 
 def _ptr(t):
@@ -238,3 +241,13 @@ def mk_selftest_quantize(x, codes, scales, s_row, stream=None):
 def mk_selftest_mma(fp4, a, a_scales, b, b_scales, K, out, stream=None):
     _check("mk_selftest_mma", _lib_mk_selftest_mma(
         int(fp4), _ptr(a), _ptr(a_scales), _ptr(b), _ptr(b_scales), K, _ptr(out), _stream(stream)))
+
+
+SCRATCH = {"q": 0, "o": 1, "x_mid": 2, "logits": 3, "p": 4, "a": 5, "z": 6, "y": 7, "idx": 8, "w": 9}
+
+
+def mk_selftest_copy_scratch(layer, which, dst):
+    """Copy a library-owned intermediate into the device tensor ``dst``."""
+    w = SCRATCH[which] if isinstance(which, str) else which
+    nbytes = dst.numel() * dst.element_size()
+    _check("mk_selftest_copy_scratch", _lib_mk_selftest_copy_scratch(layer, w, _ptr(dst), nbytes))

@@ -1,0 +1,1315 @@
+// layer.cu -- the persistent decode-layer kernel: one launch runs one decoder
+// layer's verify step (T <= 16 tokens) on every SM.
+//
+// Page "Muse Spark Open: 1,109 Tokens a Second Is a Kernel Change, Not a Model
+// Change", section "Where the kernel boundary sits, and why it stops there":
+// one launch per layer covering attention through the next layer's qkv
+// projection and KV write, one block per SM, warps with specialised roles
+// (loading, tensor cores, math).  Section "Three bills a kernel this big has to
+// pay": weights are streamed ahead of use into a shared-memory ring.
+//
+// Roles (one CTA of 256 threads per SM):
+//   warp 0      TMA producer: streams 128-row weight tiles (and NVFP4 scale
+//               factors) of every phase into a kStages-deep ring; it never
+//               waits on activations, only on the router for expert tiles.
+//   warp 1      tcgen05 MMA issuer (one thread): weights are operand A (M=128
+//               rows), the T verify tokens operand B (N=16), fp32 accumulators
+//               in tensor memory, two accumulator buffers.
+//   warps 2-3   stagers: wait for a phase's inputs, then write the token
+//               operand (RMSNorm applied, or NVFP4-quantised) into shared
+//               memory in the MMA's swizzled layout.
+//   warps 4-7   epilogue (TMEM lanes 0-127) and math: split-K fix-ups,
+//               residuals, router top-k, SwiGLU, combine; attention with
+//               warp-level MMA in the attention phase.
+// Phases are separated by grid-wide dependency counters with bounded waits.
+#include "layer.h"
+#include "ptx.cuh"
+#include "quant.cuh"
+
+namespace mk {
+
+// ------------------------------------------------------------ smem layout
+constexpr uint32_t kTileBytes = 16384;                       // 128 rows x 128 B
+constexpr uint32_t kSfBytes = 2048;                          // 4 chunks x 512 B
+constexpr uint32_t kOffA = 0;
+constexpr uint32_t kOffSF = kOffA + kStages * kTileBytes;
+constexpr uint32_t kOffB = kOffSF + kStages * kSfBytes;       // 2 operand buffers
+constexpr uint32_t kBBufBytes = 40960;
+constexpr uint32_t kBSfOff = 16384;                          // scales inside a B buffer
+constexpr uint32_t kOffMisc = kOffB + 2 * kBBufBytes;
+constexpr uint32_t kSmemBytes = kOffMisc + 8192 + 1024;     // + alignment slack
+
+struct Misc {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t bfull[2];
+  uint64_t bempty[2];
+  uint64_t accfull[2];
+  uint64_t accempty[2];
+  uint64_t route_ready;
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  uint32_t abort;
+  uint32_t epoch;
+  int n_act;                       // active experts (MoE)
+  int flag;                        // epilogue broadcast
+  int act[kMaxE];                  // active experts, ascending
+  int cnt[kMaxE];                  // tokens per expert
+  int off[kMaxE + 1];              // first slot of expert e in `slots`
+  int slots[kMaxT * kMaxK];        // slot (t*k + r) grouped by expert
+  float rnorm[kMaxT];              // stager: RMSNorm factors of the phase input
+  float srow_st[kMaxT * kMaxK];    // stager: NVFP4 row scales of the phase input
+  float srow_ep[kMaxT * kMaxK];    // epilogue: NVFP4 row scales of the phase input
+  float red[4][kMaxT];             // epilogue cross-warp reductions
+  int done[kMaxT];                 // epilogue: combine completions
+};
+static_assert(sizeof(Misc) <= 8192, "misc region");
+
+struct Smem {
+  uint8_t* base;
+  Misc* m;
+  MK_DEV uint8_t* a_tile(int s) const { return base + kOffA + s * kTileBytes; }
+  MK_DEV uint8_t* sf(int s) const { return base + kOffSF + s * kSfBytes; }
+  MK_DEV uint8_t* bbuf(int b) const { return base + kOffB + b * kBBufBytes; }
+};
+
+// ------------------------------------------------------------ errors / waits
+enum : uint32_t {
+  ERR_TIMEOUT_FULL = 0x100, ERR_TIMEOUT_EMPTY = 0x200, ERR_TIMEOUT_B = 0x300,
+  ERR_TIMEOUT_ACC = 0x400, ERR_TIMEOUT_GRID = 0x500, ERR_TIMEOUT_ROUTE = 0x600
+};
+
+MK_DEV bool aborted(const LayerParams& P, const Smem& S) {
+  return *reinterpret_cast<volatile uint32_t*>(&S.m->abort) != 0 ||
+         *reinterpret_cast<volatile uint32_t*>(P.status) != 0;
+}
+MK_DEV void raise_error(const LayerParams& P, const Smem& S, uint32_t code) {
+  atomicCAS(P.status, 0u, code | (blockIdx.x << 16) | 1u);
+  atomicExch(&S.m->abort, 1u);
+}
+
+// Bounded mbarrier wait: gives up on timeout or when the CTA/grid aborted.
+MK_DEV bool wait_bar(const LayerParams& P, const Smem& S, uint64_t* bar, uint32_t parity,
+                     uint32_t code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  uint32_t spins = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if ((++spins & 63u) == 0) {
+      if (aborted(P, S)) return false;
+      if (globaltimer() - t0 > P.timeout_ns) {
+        raise_error(P, S, code);
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
+MK_DEV uint32_t grid_target(const LayerParams& P, uint32_t epoch) {
+  return (epoch + 1u) * static_cast<uint32_t>(P.grid);
+}
+
+// One thread polls grid counter `id` until every CTA of this launch arrived.
+MK_DEV bool grid_wait(const LayerParams& P, const Smem& S, int id, uint32_t target) {
+  const uint32_t* c = P.bar_ctr + id;
+  if (static_cast<int32_t>(ld_acquire(c) - target) >= 0) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    for (int i = 0; i < 32; ++i)
+      if (static_cast<int32_t>(ld_acquire(c) - target) >= 0) return true;
+    if (aborted(P, S)) return false;
+    if (globaltimer() - t0 > P.timeout_ns) {
+      raise_error(P, S, ERR_TIMEOUT_GRID | static_cast<uint32_t>(id << 4));
+      return false;
+    }
+  }
+}
+
+MK_DEV void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+constexpr int kBarEpi = 1;     // warps 4-7
+constexpr int kBarStage = 2;   // warps 2-3
+MK_DEV void epi_sync() { named_bar(kBarEpi, 128); }
+MK_DEV void stage_sync() { named_bar(kBarStage, 64); }
+
+// ------------------------------------------------------------ bf16 helpers
+MK_DEV float bf(const __nv_bfloat16 v) { return __bfloat162float(v); }
+MK_DEV __nv_bfloat16 to_bf(float v) { return __float2bfloat16_rn(v); }
+MK_DEV float round_bf(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+MK_DEV float silu(float x) { return x / (1.0f + expf(-x)); }
+
+// ------------------------------------------------------------ phase geometry
+MK_DEV bool phase_is_gemm(int ph) {
+  return ph == PH_QKV || ph == PH_O || ph == PH_RP || ph == PH_GU || ph == PH_DOWN ||
+         ph == PH_UNPOOL || ph == PH_NQKV;
+}
+
+MK_DEV bool phase_active(const LayerParams& P, int ph) {
+  switch (ph) {
+    case PH_QKV: return P.first_layer != 0;
+    case PH_GU: case PH_UNPOOL: return P.moe != 0;
+    case PH_NQKV: return P.fuse_next != 0;
+    default: return true;
+  }
+}
+
+MK_DEV int phase_units(const LayerParams& P, const Smem& S, int ph) {
+  switch (ph) {
+    case PH_QKV: case PH_NQKV: return P.tiles_qkv * P.ks_qkv;
+    case PH_O: return P.tiles_o * P.ks_o;
+    case PH_RP: return P.moe ? (P.tiles_router + P.tiles_pool) * P.ks_rp : P.tiles_dgu * P.ks_dgu;
+    case PH_GU: return S.m->n_act * (P.I / 128);
+    case PH_DOWN: return P.moe ? S.m->n_act * (P.P / 128) : P.tiles_ddown * P.ks_ddown;
+    case PH_UNPOOL: return P.tiles_unpool * P.ks_unpool;
+    case PH_ATTN: return P.Hkv * P.attn_chunks;
+    case PH_MERGE: return P.T * P.Hq;
+  }
+  return 0;
+}
+
+// First unit of this CTA in a phase (units are dealt round-robin, rotated by
+// phase so that the CTAs holding a phase's extra units change).
+MK_DEV int first_unit(const LayerParams& P, int ph) {
+  const int rot = (ph * 37) % P.grid;
+  return (static_cast<int>(blockIdx.x) + P.grid - rot) % P.grid;
+}
+
+// The grid counter a phase's token operand waits for (-1: none).
+MK_DEV int phase_dep(const LayerParams& P, int ph) {
+  switch (ph) {
+    case PH_O: return BAR_MERGE;
+    case PH_RP: return BAR_O;
+    case PH_GU: return BAR_RP;
+    case PH_DOWN: return P.moe ? BAR_GU : BAR_RP;
+    case PH_UNPOOL: return BAR_DOWN;
+    case PH_NQKV: return BAR_X;
+  }
+  return -1;
+}
+// The grid counter the epilogue arrives on when a phase is done.
+MK_DEV int phase_arrive(const LayerParams& P, int ph) {
+  switch (ph) {
+    case PH_QKV: return BAR_QKV;
+    case PH_ATTN: return BAR_ATTN;
+    case PH_MERGE: return BAR_MERGE;
+    case PH_O: return BAR_O;
+    case PH_RP: return BAR_RP;
+    case PH_GU: return BAR_GU;
+    case PH_DOWN: return P.moe ? BAR_DOWN : BAR_X;
+    case PH_UNPOOL: return BAR_X;
+    case PH_NQKV: return BAR_END;
+  }
+  return -1;
+}
+MK_DEV int final_barrier(const LayerParams& P) { return P.fuse_next ? BAR_END : BAR_X; }
+
+struct Unit {
+  const CUtensorMap* map[2];
+  const uint8_t* sf[2];  // repacked scales of K-block 0 (NVFP4)
+  int pair;              // 1 or 2 weight matrices (gate + up)
+  int fp4;
+  int row0;              // TMA row of the tile
+  int x0;                // TMA x of K-block 0 (elements for bf16, bytes for NVFP4)
+  int nkb;               // K-blocks of 128 bytes per row
+  int tile;              // 128-row tile index within its matrix
+  int ks;                // K-split index
+  int ksplit;
+  int expert;            // NVFP4 units
+  int router;            // PH_RP (MoE): 1 = router tile, 0 = pooler tile
+  int N;                 // rows of the weight matrix (outputs)
+  int K;                 // inputs of the weight matrix
+  int col_tile;          // tile index in the phase's split-K partial columns
+  int col_tiles;         // tiles in the phase's split-K partial columns
+};
+
+MK_DEV Unit make_unit(const LayerParams& P, const Smem& S, int ph, int u) {
+  Unit U{};
+  U.pair = 1;
+  U.map[1] = nullptr;
+  U.sf[0] = U.sf[1] = nullptr;
+  auto bf16_unit = [&](const CUtensorMap* m, int N, int K, int ks_count, int tile_base) {
+    U.map[0] = m;
+    U.fp4 = 0;
+    U.col_tile = u / ks_count;
+    U.tile = U.col_tile - tile_base;
+    U.ks = u % ks_count;
+    U.ksplit = ks_count;
+    U.row0 = U.tile * 128;
+    const int kc = K / ks_count;
+    U.x0 = U.ks * kc;
+    U.nkb = kc / 64;
+    U.N = N;
+    U.K = K;
+  };
+  switch (ph) {
+    case PH_QKV:
+      bf16_unit(&P.tm_qkv, P.Nqkv, P.H, P.ks_qkv, 0);
+      U.col_tiles = P.tiles_qkv;
+      break;
+    case PH_NQKV:
+      bf16_unit(&P.tm_nqkv, P.Nqkv, P.H, P.ks_qkv, 0);
+      U.col_tiles = P.tiles_qkv;
+      break;
+    case PH_O:
+      bf16_unit(&P.tm_o, P.H, P.Hq * P.d, P.ks_o, 0);
+      U.col_tiles = P.tiles_o;
+      break;
+    case PH_UNPOOL:
+      bf16_unit(&P.tm_unpool, P.H, P.P, P.ks_unpool, 0);
+      U.col_tiles = P.tiles_unpool;
+      break;
+    case PH_RP:
+      U.col_tiles = P.moe ? P.tiles_router + P.tiles_pool : P.tiles_dgu;
+      if (P.moe) {
+        if (u < P.tiles_router * P.ks_rp) {
+          bf16_unit(&P.tm_router, P.E, P.H, P.ks_rp, 0);
+          U.router = 1;
+        } else {
+          bf16_unit(&P.tm_pool, P.P, P.H, P.ks_rp, P.tiles_router);
+          U.router = 0;
+        }
+      } else {
+        bf16_unit(&P.tm_gate, P.F, P.H, P.ks_dgu, 0);
+        U.map[1] = &P.tm_up;
+        U.pair = 2;
+      }
+      break;
+    case PH_DOWN:
+      if (!P.moe) {
+        bf16_unit(&P.tm_down, P.H, P.F, P.ks_ddown, 0);
+        U.col_tiles = P.tiles_ddown;
+        break;
+      }
+      [[fallthrough]];
+    case PH_GU: {
+      const bool gu = ph == PH_GU;
+      const int N = gu ? P.I : P.P, K = gu ? P.P : P.I;
+      const int tiles = N / 128;
+      const int e = S.m->act[u / tiles];
+      U.fp4 = 1;
+      U.expert = e;
+      U.tile = u % tiles;
+      U.ks = 0;
+      U.ksplit = 1;
+      U.row0 = e * N + U.tile * 128;
+      U.x0 = 0;
+      U.nkb = (K + 255) / 256;
+      U.N = N;
+      U.K = K;
+      const size_t sf_off = (static_cast<size_t>(e) * tiles + U.tile) * U.nkb * kSfBytes;
+      if (gu) {
+        U.map[0] = &P.tm_gate;
+        U.map[1] = &P.tm_up;
+        U.pair = 2;
+        U.sf[0] = P.sf_gate + sf_off;
+        U.sf[1] = P.sf_up + sf_off;
+      } else {
+        U.map[0] = &P.tm_down;
+        U.sf[0] = P.sf_down + sf_off;
+      }
+      break;
+    }
+  }
+  return U;
+}
+
+// ------------------------------------------------------------ routing table
+// One warp: group the (token, rank) slots by expert, deterministically
+// (experts ascending, slots ascending within an expert).
+MK_DEV void build_routing(const LayerParams& P, const Smem& S) {
+  Misc* m = S.m;
+  const int lane = lane_id();
+  for (int e = lane; e < P.E; e += 32) m->cnt[e] = 0;
+  __syncwarp();
+  const int nslot = P.T * P.topk;
+  for (int s0 = 0; s0 < nslot; s0 += 32) {
+    const int s = s0 + lane;
+    const int e = s < nslot ? P.idx[s] : -1 - lane;
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    if (s < nslot && (peers & ((1u << lane) - 1)) == 0) m->cnt[e] += __popc(peers);
+    __syncwarp();
+  }
+  // exclusive scan of cnt -> off, and the active list
+  int base = 0, nact = 0;
+  for (int e0 = 0; e0 < P.E; e0 += 32) {
+    const int e = e0 + lane;
+    const int c = e < P.E ? m->cnt[e] : 0;
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const uint32_t act = __ballot_sync(0xffffffffu, c > 0);
+    if (e < P.E) {
+      m->off[e] = base + incl - c;
+      if (c > 0) m->act[nact + __popc(act & ((1u << lane) - 1))] = e;
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+    nact += __popc(act);
+  }
+  if (lane == 0) {
+    m->off[P.E] = base;
+    m->n_act = nact;
+  }
+  __syncwarp();
+  // place slots: rank within the expert = earlier slots with the same expert
+  for (int e = lane; e < P.E; e += 32) m->cnt[e] = 0;
+  __syncwarp();
+  for (int s0 = 0; s0 < nslot; s0 += 32) {
+    const int s = s0 + lane;
+    const int e = s < nslot ? P.idx[s] : -1 - lane;
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    if (s < nslot) {
+      const int rank = __popc(peers & ((1u << lane) - 1));
+      m->slots[m->off[e] + m->cnt[e] + rank] = s;
+    }
+    __syncwarp();
+    if (s < nslot && (peers & ((1u << lane) - 1)) == 0) m->cnt[e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+// ============================================================ producer (warp 0)
+MK_DEV void run_producer(const LayerParams& P, const Smem& S) {
+  Misc* m = S.m;
+  const uint64_t pol = policy_evict_first();
+  uint32_t stage = 0, phase = 0;
+  bool route_known = false;
+  bool ok = true;
+  for (int ph = 0; ph < PH_COUNT && ok; ++ph) {
+    if (!phase_is_gemm(ph) || !phase_active(P, ph)) continue;
+    if (P.moe && ph == PH_GU && !route_known) {
+      if (!wait_bar(P, S, &m->route_ready, 0, ERR_TIMEOUT_ROUTE)) { ok = false; break; }
+      route_known = true;
+    }
+    const int n = phase_units(P, S, ph);
+    for (int u = first_unit(P, ph); u < n && ok; u += P.grid) {
+      const Unit U = make_unit(P, S, ph, u);
+      const uint32_t bytes = kTileBytes + (U.fp4 ? kSfBytes : 0);
+      for (int kb = 0; kb < U.nkb && ok; ++kb) {
+        for (int j = 0; j < U.pair; ++j) {
+          if (!wait_bar(P, S, &m->empty[stage], phase ^ 1, ERR_TIMEOUT_EMPTY)) { ok = false; break; }
+          mbar_arrive_expect_tx(&m->full[stage], bytes);
+          const int x = U.x0 + kb * (U.fp4 ? 128 : 64);
+          tma_load_2d(S.a_tile(stage), U.map[j], &m->full[stage], x, U.row0, pol);
+          if (U.fp4) bulk_load(S.sf(stage), U.sf[j] + kb * kSfBytes, kSfBytes, &m->full[stage], pol);
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+      }
+    }
+  }
+  // Drain: every issued copy must land before the CTA may exit.
+  for (int s = 0; s < kStages; ++s) {
+    // the most recent use of stage s had parity (phase ^ (s >= stage ? 1 : 0))
+    const uint32_t par = s < static_cast<int>(stage) ? phase : phase ^ 1;
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(&m->full[s], par)) {
+      if (globaltimer() - t0 > P.timeout_ns) break;
+    }
+  }
+}
+
+// ============================================================ MMA (warp 1)
+MK_DEV void run_mma(const LayerParams& P, const Smem& S) {
+  Misc* m = S.m;
+  const uint32_t tbase = m->tmem_base;
+  uint32_t stage = 0, phase = 0, acc_ph[2] = {0, 0}, b_ph[2] = {0, 0};
+  uint32_t ucount = 0, sfreg = 0;
+  bool ok = true;
+  bool route_known = false;
+  for (int ph = 0; ph < PH_COUNT && ok; ++ph) {
+    if (!phase_is_gemm(ph) || !phase_active(P, ph)) continue;
+    if (P.moe && ph == PH_GU && !route_known) {
+      if (!wait_bar(P, S, &m->route_ready, 0, ERR_TIMEOUT_ROUTE)) { ok = false; break; }
+      route_known = true;
+    }
+    const int n = phase_units(P, S, ph);
+    for (int u = first_unit(P, ph); u < n && ok; u += P.grid) {
+      const Unit U = make_unit(P, S, ph, u);
+      const uint32_t b = ucount & 1;
+      if (!wait_bar(P, S, &m->accempty[b], acc_ph[b] ^ 1, ERR_TIMEOUT_ACC)) { ok = false; break; }
+      if (!wait_bar(P, S, &m->bfull[b], b_ph[b], ERR_TIMEOUT_B)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t acc = tbase + 32 * b;
+      uint8_t* bb = S.bbuf(b);
+      for (int kb = 0; kb < U.nkb && ok; ++kb) {
+        for (int j = 0; j < U.pair; ++j) {
+          if (!wait_bar(P, S, &m->full[stage], phase, ERR_TIMEOUT_FULL)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t da = sdesc_kmajor_sw128(smem_u32(S.a_tile(stage)));
+          const uint64_t db = sdesc_kmajor_sw128(smem_u32(bb + kb * 2048));
+          const uint32_t d = acc + 16 * j;
+          if (U.fp4) {
+            const uint32_t sfa = tbase + 64 + 32 * sfreg, sfb = sfa + 16;
+            sfreg = (sfreg + 1) & 3;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              tmem_cp_sf(sfa + 4 * c, sdesc_sf_chunk(smem_u32(S.sf(stage) + c * 512)));
+              tmem_cp_sf(sfb + 4 * c,
+                         sdesc_sf_chunk(smem_u32(bb + kBSfOff + (kb * 4 + c) * 512)));
+            }
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_nvf4(d, da + 2 * kk, db + 2 * kk, idesc_nvf4(128, kMaxT), sfa + 4 * kk,
+                       sfb + 4 * kk, (kb | kk) != 0);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16(d, da + 2 * kk, db + 2 * kk, idesc_bf16(128, kMaxT), (kb | kk) != 0);
+          }
+          mma_commit(&m->empty[stage]);
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (!ok) break;
+      mma_commit(&m->accfull[b]);
+      mma_commit(&m->bempty[b]);
+      acc_ph[b] ^= 1;
+      b_ph[b] ^= 1;
+      ++ucount;
+    }
+  }
+  // all issued tensor-core work completes before TMEM is released
+  mma_commit(&m->mma_done);
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(&m->mma_done, 0)) {
+    if (globaltimer() - t0 > P.timeout_ns) break;
+  }
+}
+
+// ============================================================ stagers (warps 2-3)
+// Token operand of a bf16 unit: rows t < T of src[t][k0 .. k0 + 64*nkb),
+// optionally x * rnorm[t] * gain[k] rounded to bf16; rows >= T are zero.
+MK_DEV void stage_bf16(const LayerParams& P, const Smem& S, uint8_t* bb, const __nv_bfloat16* src,
+                       int ld, int k0, int nkb, const __nv_bfloat16* gain) {
+  const int tid = threadIdx.x - 64;
+  const int chunks = nkb * 8;  // 16-byte chunks per row
+  for (int i = tid; i < kMaxT * chunks; i += 64) {
+    const int t = i / chunks, c = i % chunks;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (t < P.T) {
+      const int k = k0 + c * 8;
+      v = *reinterpret_cast<const uint4*>(src + static_cast<size_t>(t) * ld + k);
+      if (gain) {
+        const uint4 g = *reinterpret_cast<const uint4*>(gain + k);
+        const float r = S.m->rnorm[t];
+        uint32_t* pv = reinterpret_cast<uint32_t*>(&v);
+        const uint32_t* pg = reinterpret_cast<const uint32_t*>(&g);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const float x0 = __uint_as_float(pv[w] << 16), x1 = __uint_as_float(pv[w] & 0xFFFF0000u);
+          const float g0 = __uint_as_float(pg[w] << 16), g1 = __uint_as_float(pg[w] & 0xFFFF0000u);
+          const __nv_bfloat162 o = __floats2bfloat162_rn(x0 * r * g0, x1 * r * g1);
+          pv[w] = *reinterpret_cast<const uint32_t*>(&o);
+        }
+      }
+    }
+    const int byte = c * 16;
+    *reinterpret_cast<uint4*>(bb + (byte >> 7) * 2048 + sw128_offset(t, byte & 127)) = v;
+  }
+}
+
+// Quantiser sink with a given row scale.
+template <class Sink>
+MK_DEV void quantize_row_given_srow(const __nv_bfloat16* row, int K, float s_row, Sink& sink) {
+  const int lane = lane_id();
+  const float d6 = __fmul_rn(6.0f, s_row);
+  for (int b = lane; b < (K >> 4); b += 32) {
+    float x[16];
+    load_bf16x16(row + b * 16, x);
+    float a16 = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) a16 = fmaxf(a16, fabsf(x[i]));
+    const uint32_t sb = cvt_e4m3(__fdiv_rn(a16, d6));
+    const float sbf = e4m3_to_float(sb);
+    uint32_t w0 = 0, w1 = 0;
+    if (sbf > 0.f) {
+      const float c = __fmul_rn(sbf, s_row);
+      float r[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) r[i] = __fdiv_rn(x[i], c);
+      w0 = cvt_e2m1x4(r[0], r[1], r[2], r[3]) | (cvt_e2m1x4(r[4], r[5], r[6], r[7]) << 16);
+      w1 = cvt_e2m1x4(r[8], r[9], r[10], r[11]) | (cvt_e2m1x4(r[12], r[13], r[14], r[15]) << 16);
+    }
+    sink.put(b, w0, w1, sb);
+  }
+}
+
+// Token operand of an NVFP4 expert unit: row i = the i-th slot routed to the
+// expert, quantised from bf16 rows of `src` (ld elements apart).
+MK_DEV void stage_fp4(const LayerParams& P, const Smem& S, uint8_t* bb, const Unit& U, bool gu) {
+  Misc* m = S.m;
+  const int warp = (threadIdx.x >> 5) - 2;  // 0..1
+  const int e = U.expert;
+  const int n = m->off[e + 1] - m->off[e];
+  const int K = U.K;
+  // K-block padding beyond K must read as zero codes and zero scales
+  if (K % 256) {
+    const int tid = threadIdx.x - 64;
+    const int kb = K / 256, pad_from = (K % 256) / 2;  // bytes of the last K-block row in use
+    for (int i = tid; i < kMaxT * 128; i += 64) {
+      const int r = i / 128, byte = i % 128;
+      if (byte >= pad_from) bb[kb * 2048 + sw128_offset(r, byte)] = 0;
+    }
+    for (int i = tid; i < 512 * (4 - (K % 256) / 64); i += 64)
+      bb[kBSfOff + (kb * 4 + (K % 256) / 64) * 512 + i] = 0;
+  }
+  for (int i = warp; i < n; i += 2) {
+    const int s = m->slots[m->off[e] + i];
+    const int t = s / P.topk;
+    const __nv_bfloat16* row = gu ? P.p_buf + static_cast<size_t>(t) * P.P
+                                  : P.a_buf + static_cast<size_t>(s) * P.I;
+    OperandSink sink{bb, bb + kBSfOff, static_cast<uint32_t>(i)};
+    quantize_row_given_srow(row, K, gu ? m->srow_st[t] : m->srow_st[s], sink);
+  }
+}
+
+MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
+  Misc* m = S.m;
+  const int tid = threadIdx.x - 64;  // 0..63
+  const int warp = tid >> 5;
+  const uint32_t target = grid_target(P, epoch);
+  uint32_t b_ph[2] = {0, 0}, ucount = 0;
+  bool ok = true;
+  // RMSNorm factors of x_in (first layer)
+  if (P.first_layer) {
+    for (int t = warp; t < P.T; t += 2) {
+      const __nv_bfloat16* x = P.x_in + static_cast<size_t>(t) * P.H;
+      float s = 0.f;
+      for (int k = lane_id() * 8; k < P.H; k += 256) {
+        const uint4 v = *reinterpret_cast<const uint4*>(x + k);
+        const uint32_t* pv = reinterpret_cast<const uint32_t*>(&v);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const float a = __uint_as_float(pv[w] << 16), b2 = __uint_as_float(pv[w] & 0xFFFF0000u);
+          s += a * a + b2 * b2;
+        }
+      }
+      s = warp_sum(s);
+      if (lane_id() == 0) m->rnorm[t] = 1.0f / sqrtf(s / P.H + P.eps);
+    }
+    stage_sync();
+  }
+  for (int ph = 0; ph < PH_COUNT && ok; ++ph) {
+    if (!phase_is_gemm(ph) || !phase_active(P, ph)) continue;
+    const int dep = phase_dep(P, ph);
+    if (dep >= 0) {
+      if (tid == 0 && !grid_wait(P, S, dep, target)) atomicExch(&m->abort, 1u);
+      stage_sync();
+      if (aborted(P, S)) { ok = false; break; }
+    }
+    // per-phase inputs of the token operand
+    if (ph == PH_RP || ph == PH_NQKV) {
+      const float* ssq = ph == PH_RP ? P.ssq_mid : P.ssq_out;
+      if (tid < P.T) {
+        float s = 0.f;
+        for (int j = 0; j < P.H / 128; ++j) s += ssq[j * kMaxT + tid];
+        m->rnorm[tid] = 1.0f / sqrtf(s / P.H + P.eps);
+      }
+    } else if (ph == PH_GU) {
+      if (warp == 0) {
+        build_routing(P, S);
+        __syncwarp();
+        if (lane_id() == 0) mbar_arrive(&m->route_ready);
+      }
+      if (tid < P.T) {
+        float a = 0.f;
+        for (int j = 0; j < P.P / 128; ++j) a = fmaxf(a, P.pamax[j * kMaxT + tid]);
+        m->srow_st[tid] = a > 0.f ? __fdiv_rn(a, 2688.0f) : 1.0f;
+      }
+    } else if (ph == PH_DOWN && P.moe) {
+      for (int s = tid; s < P.T * P.topk; s += 64) {
+        float a = 0.f;
+        for (int j = 0; j < P.I / 128; ++j) a = fmaxf(a, P.aamax[s * (P.I / 128) + j]);
+        m->srow_st[s] = a > 0.f ? __fdiv_rn(a, 2688.0f) : 1.0f;
+      }
+    }
+    stage_sync();
+    const int n = phase_units(P, S, ph);
+    for (int u = first_unit(P, ph); u < n && ok; u += P.grid) {
+      const Unit U = make_unit(P, S, ph, u);
+      const uint32_t b = ucount & 1;
+      if (!wait_bar(P, S, &m->bempty[b], b_ph[b] ^ 1, ERR_TIMEOUT_B)) { ok = false; break; }
+      uint8_t* bb = S.bbuf(b);
+      switch (ph) {
+        case PH_QKV: stage_bf16(P, S, bb, P.x_in, P.H, U.x0, U.nkb, P.attn_norm_w); break;
+        case PH_NQKV: stage_bf16(P, S, bb, P.x_out, P.H, U.x0, U.nkb, P.next_attn_norm_w); break;
+        case PH_O: stage_bf16(P, S, bb, P.o_buf, P.Hq * P.d, U.x0, U.nkb, nullptr); break;
+        case PH_RP: stage_bf16(P, S, bb, P.xmid, P.H, U.x0, U.nkb, P.ffn_norm_w); break;
+        case PH_UNPOOL: stage_bf16(P, S, bb, P.y_buf, P.P, U.x0, U.nkb, nullptr); break;
+        case PH_GU: stage_fp4(P, S, bb, U, true); break;
+        case PH_DOWN:
+          if (P.moe) stage_fp4(P, S, bb, U, false);
+          else stage_bf16(P, S, bb, P.a_buf, P.F, U.x0, U.nkb, nullptr);
+          break;
+      }
+      fence_proxy_async_smem();
+      stage_sync();
+      if (tid == 0) mbar_arrive(&m->bfull[b]);
+      b_ph[b] ^= 1;
+      ++ucount;
+    }
+  }
+}
+
+// ============================================================ epilogue (warps 4-7)
+// Cross-warp reduction over the 128 epilogue threads of 16 per-token values:
+// returns, in thread t (< 16), the sum (or max) for token t.
+template <bool kMax>
+MK_DEV float epi_reduce16(const Smem& S, float (&v)[kMaxT], int et) {
+  const int q = et >> 5;
+#pragma unroll
+  for (int t = 0; t < kMaxT; ++t) {
+    float x = v[t];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float y = __shfl_xor_sync(0xffffffffu, x, o);
+      x = kMax ? fmaxf(x, y) : x + y;
+    }
+    if (lane_id() == 0) S.m->red[q][t] = x;
+  }
+  epi_sync();
+  float r = 0.f;
+  if (et < kMaxT) {
+    r = S.m->red[0][et];
+    for (int w = 1; w < 4; ++w) r = kMax ? fmaxf(r, S.m->red[w][et]) : r + S.m->red[w][et];
+  }
+  epi_sync();
+  return r;
+}
+
+// Router: top-k of the float32 logits (descending, ties to the lower index),
+// softmax over all experts, combine weights.  One warp per token.
+MK_DEV void router_topk(const LayerParams& P, int et) {
+  const int w = et >> 5, lane = lane_id();
+  for (int t = w; t < P.T; t += 4) {
+    const float* lg = P.logits + static_cast<size_t>(t) * kMaxE;
+    float v[kMaxE / 32];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kMaxE / 32; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = e < P.E ? lg[e] : -INFINITY;
+      mx = fmaxf(mx, v[i]);
+    }
+    mx = warp_max(mx);
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < kMaxE / 32; ++i)
+      if (lane + 32 * i < P.E) sum += expf(v[i] - mx);
+    sum = warp_sum(sum);
+    uint32_t taken = 0;
+    float sel_w[kMaxK];
+    int sel_i[kMaxK];
+    for (int r = 0; r < P.topk; ++r) {
+      float best = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < kMaxE / 32; ++i) {
+        const int e = lane + 32 * i;
+        if (e < P.E && !((taken >> i) & 1u) && (v[i] > best || (v[i] == best && e < bi))) {
+          best = v[i];
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; }
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      sel_i[r] = bi;
+      sel_w[r] = expf(best - mx) / sum;
+    }
+    if (P.renorm) {
+      float s = 0.f;
+      for (int r = 0; r < P.topk; ++r) s += sel_w[r];
+      for (int r = 0; r < P.topk; ++r) sel_w[r] = sel_w[r] / s;
+    }
+    if (lane < P.topk) {
+      int ii = 0;
+      float ww = 0.f;
+      for (int r = 0; r < P.topk; ++r)
+        if (r == lane) { ii = sel_i[r]; ww = sel_w[r]; }
+      P.idx[t * P.topk + lane] = ii;
+      P.wts[t * P.topk + lane] = ww;
+      if (P.topk_idx_out) P.topk_idx_out[t * P.topk + lane] = ii;
+      if (P.topk_w_out) P.topk_w_out[t * P.topk + lane] = ww;
+    }
+  }
+}
+
+// Final values of one 128-row tile of a bf16 phase: acc[j][t] for the row
+// (feature) f of this thread.
+MK_DEV void epi_bf16_final(const LayerParams& P, const Smem& S, int ph, const Unit& U, int et,
+                           float (&g)[kMaxT], float (&u)[kMaxT]) {
+  const int f = U.row0 + et;
+  const bool valid = f < U.N;
+  switch (ph) {
+    case PH_QKV:
+    case PH_NQKV: {
+      if (!valid) break;
+      __nv_bfloat16* qdst = ph == PH_QKV ? P.q_buf : P.q_out;
+      __nv_bfloat16* kc = ph == PH_QKV ? P.k_cache : P.nk_cache;
+      __nv_bfloat16* vc = ph == PH_QKV ? P.v_cache : P.nv_cache;
+      const int nq = P.Hq * P.d, nk = P.Hkv * P.d;
+      for (int t = 0; t < P.T; ++t) {
+        const __nv_bfloat16 v = to_bf(g[t]);
+        if (f < nq) qdst[static_cast<size_t>(t) * nq + f] = v;
+        else if (f < nq + nk) kc[static_cast<size_t>(P.ctx + t) * nk + (f - nq)] = v;
+        else vc[static_cast<size_t>(P.ctx + t) * nk + (f - nq - nk)] = v;
+      }
+      break;
+    }
+    case PH_O:
+    case PH_UNPOOL:
+    case PH_DOWN: {  // residual: x = bf16(res + acc); sum-of-squares partial
+      const __nv_bfloat16* res = ph == PH_O ? P.x_in : P.xmid;
+      __nv_bfloat16* dst = ph == PH_O ? P.xmid : P.x_out;
+      float sq[kMaxT];
+#pragma unroll
+      for (int t = 0; t < kMaxT; ++t) {
+        sq[t] = 0.f;
+        if (valid && t < P.T) {
+          const size_t o = static_cast<size_t>(t) * P.H + f;
+          const float x = round_bf(bf(res[o]) + g[t]);
+          dst[o] = to_bf(x);
+          sq[t] = x * x;
+        }
+      }
+      const float r = epi_reduce16<false>(S, sq, et);
+      if (et < P.T) (ph == PH_O ? P.ssq_mid : P.ssq_out)[U.tile * kMaxT + et] = r;
+      break;
+    }
+    case PH_RP: {
+      if (!P.moe) {  // dense SwiGLU
+        if (valid)
+          for (int t = 0; t < P.T; ++t)
+            P.a_buf[static_cast<size_t>(t) * P.F + f] = to_bf(silu(g[t]) * u[t]);
+        break;
+      }
+      if (U.router) {
+        if (valid)
+          for (int t = 0; t < P.T; ++t) P.logits[static_cast<size_t>(t) * kMaxE + f] = g[t];
+      } else {
+        float am[kMaxT];
+#pragma unroll
+        for (int t = 0; t < kMaxT; ++t) {
+          am[t] = 0.f;
+          if (valid && t < P.T) {
+            const float x = round_bf(g[t]);
+            P.p_buf[static_cast<size_t>(t) * P.P + f] = to_bf(x);
+            am[t] = fabsf(x);
+          }
+        }
+        const float r = epi_reduce16<true>(S, am, et);
+        if (et < P.T) P.pamax[U.tile * kMaxT + et] = r;
+      }
+      break;
+    }
+  }
+}
+
+// Epilogue of one GEMM unit.
+MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Unit& U,
+                          uint32_t b, uint32_t& acc_ph_b, int et) {
+  Misc* m = S.m;
+  if (!wait_bar(P, S, &m->accfull[b], acc_ph_b, ERR_TIMEOUT_ACC)) return false;
+  acc_ph_b ^= 1;
+  tc_fence_after();
+  const int q = et >> 5;
+  const uint32_t taddr = m->tmem_base + (static_cast<uint32_t>(32 * q) << 16) + 32 * b;
+  float g[kMaxT], u[kMaxT];
+  tmem_ld16(taddr, g);
+  if (U.pair == 2) tmem_ld16(taddr + 16, u);
+  tc_fence_before();
+  __syncwarp();
+  if (lane_id() == 0) mbar_arrive(&m->accempty[b]);
+
+  if (U.fp4) {
+    const int e = U.expert;
+    const int n = m->off[e + 1] - m->off[e];
+    const int f = U.tile * 128 + et;
+    if (ph == PH_GU) {
+      const float tg = P.ts_gate[e], tu = P.ts_up[e];
+      float am[kMaxT];
+#pragma unroll
+      for (int i = 0; i < kMaxT; ++i) {
+        am[i] = 0.f;
+        if (i < n) {
+          const int s = m->slots[m->off[e] + i];
+          const float sr = m->srow_ep[s / P.topk];
+          const float gv = g[i] * sr * tg, uv = u[i] * sr * tu;
+          const float a = round_bf(silu(gv) * uv);
+          P.a_buf[static_cast<size_t>(s) * P.I + f] = to_bf(a);
+          am[i] = fabsf(a);
+        }
+      }
+      const float r = epi_reduce16<true>(S, am, et);
+      if (et < n) P.aamax[m->slots[m->off[e] + et] * (P.I / 128) + U.tile] = r;
+    } else {
+      const float td = P.ts_down[e];
+      for (int i = 0; i < n; ++i) {
+        const int s = m->slots[m->off[e] + i];
+        P.z_buf[static_cast<size_t>(s) * P.P + f] = to_bf(g[i] * m->srow_ep[s] * td);
+      }
+      __threadfence();
+      epi_sync();
+      const int tiles = P.P / 128;
+      if (et < n) {
+        const int s = m->slots[m->off[e] + et];
+        const int t = s / P.topk;
+        uint32_t* c = P.comb_ctr + t * tiles + U.tile;
+        const uint32_t old = atomicAdd(c, 1u);
+        const bool last = old == static_cast<uint32_t>(P.topk - 1);
+        if (last) *c = 0;
+        m->done[et] = last ? t : -1;
+      }
+      epi_sync();
+      for (int i = 0; i < n; ++i) {
+        const int t = m->done[i];
+        if (t < 0) continue;
+        __threadfence();
+        float acc = 0.f;
+        for (int r = 0; r < P.topk; ++r)
+          acc += P.wts[t * P.topk + r] *
+                 bf(P.z_buf[static_cast<size_t>(t * P.topk + r) * P.P + f]);
+        P.y_buf[static_cast<size_t>(t) * P.P + f] = to_bf(acc);
+      }
+      epi_sync();
+    }
+    return true;
+  }
+
+  // bf16 phase: split-K partials + fix-up by the last arriving unit of a tile
+  if (U.ksplit > 1) {
+    // partials: part[ks][j][t][col], col = col_tile * 128 + row in tile
+    const size_t Npad = static_cast<size_t>(U.col_tiles) * 128;
+    const int col = U.col_tile * 128 + et;
+    for (int j = 0; j < U.pair; ++j) {
+      float* dst = P.part + (static_cast<size_t>(U.ks * U.pair + j) * kMaxT) * Npad + col;
+      for (int t = 0; t < P.T; ++t) dst[static_cast<size_t>(t) * Npad] = j ? u[t] : g[t];
+    }
+    __threadfence();
+    epi_sync();
+    if (et == 0) {
+      uint32_t* c = P.fix_ctr + ph * 256 + U.col_tile;
+      const uint32_t old = atomicAdd(c, 1u);
+      const bool last = old == static_cast<uint32_t>(U.ksplit - 1);
+      if (last) *c = 0;
+      m->flag = last;
+    }
+    epi_sync();
+    if (!m->flag) return true;
+    __threadfence();
+    for (int j = 0; j < U.pair; ++j) {
+      const float* src = P.part + (static_cast<size_t>(j) * kMaxT) * Npad + col;
+      for (int t = 0; t < P.T; ++t) {
+        float acc = 0.f;
+        for (int ks = 0; ks < U.ksplit; ++ks)
+          acc += src[(static_cast<size_t>(ks * U.pair) * kMaxT + t) * Npad];
+        (j ? u : g)[t] = acc;
+      }
+    }
+  }
+  epi_bf16_final(P, S, ph, U, et, g, u);
+  if (ph == PH_RP && P.moe && U.router) {
+    // the last finished router tile computes the top-k for every token
+    __threadfence();
+    epi_sync();
+    if (et == 0) {
+      const uint32_t old = atomicAdd(P.misc_ctr, 1u);
+      const bool last = old == static_cast<uint32_t>(P.tiles_router - 1);
+      if (last) *P.misc_ctr = 0;
+      m->flag = last;
+    }
+    epi_sync();
+    if (m->flag) {
+      __threadfence();
+      router_topk(P, et);
+    }
+  }
+  return true;
+}
+
+// ------------------------------------------------------------ attention (warps 4-7)
+MK_DEV void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+MK_DEV void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+MK_DEV void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+MK_DEV void cp_async16(uint32_t dst, const void* src, bool valid) {
+  const int n = valid ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n)
+               : "memory");
+}
+MK_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+MK_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+MK_DEV uint32_t pack_bf16(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Row r, 16-byte chunk c of a [64][D] bf16 tile: chunks XOR-swizzled by r % 8.
+template <int D>
+MK_DEV uint32_t tile_off(int r, int c) {
+  return static_cast<uint32_t>(r * (D * 2) + ((c ^ (r & 7)) << 4));
+}
+
+// One unit: KV head g, positions [lo, hi).  Each warp owns q head 4g + w and
+// the T tokens (16 rows); flash-style online softmax in the log2 domain.
+template <int D>
+MK_DEV void attention_unit(const LayerParams& P, const Smem& S, int g, int lo, int hi, int chunk_id,
+                           int et) {
+  constexpr int kChunks = D / 8;  // 16-byte chunks per row
+  uint8_t* sQ = S.bbuf(0);
+  uint8_t* sK[2] = {sQ + 64 * D * 2, sQ + 64 * D * 2 + 2 * 64 * D * 2};
+  uint8_t* sV[2] = {sK[0] + 64 * D * 2, sK[1] + 64 * D * 2};
+  const int w = et >> 5, lane = lane_id();
+  const int Hkv = P.Hkv;
+  const size_t kv_row = static_cast<size_t>(Hkv) * D;  // elements per position
+  const __nv_bfloat16* qsrc = P.first_layer ? P.q_buf : P.q_in;
+  const int qld = P.Hq * D;
+
+  // Q tile: row = w*16 + t (q head 4g+w, token t)
+  for (int i = et; i < 64 * kChunks; i += 128) {
+    const int r = i / kChunks, c = i % kChunks;
+    const int hl = r >> 4, t = r & 15;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (t < P.T)
+      v = *reinterpret_cast<const uint4*>(qsrc + static_cast<size_t>(t) * qld +
+                                          (4 * g + hl) * D + c * 8);
+    *reinterpret_cast<uint4*>(sQ + tile_off<D>(r, c)) = v;
+  }
+  auto load_kv = [&](int buf, int p0) {
+    for (int i = et; i < 64 * kChunks; i += 128) {
+      const int r = i / kChunks, c = i % kChunks;
+      const int pos = p0 + r;
+      const bool valid = pos < hi;
+      const size_t off = static_cast<size_t>(valid ? pos : lo) * kv_row + g * D + c * 8;
+      cp_async16(smem_u32(sK[buf] + tile_off<D>(r, c)), P.k_cache + off, valid);
+      cp_async16(smem_u32(sV[buf] + tile_off<D>(r, c)), P.v_cache + off, valid);
+    }
+    cp_async_commit();
+  };
+  load_kv(0, lo);
+  epi_sync();
+
+  // Q fragments of this warp (rows w*16 .. w*16+15)
+  uint32_t qa[D / 16][4];
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    const int r = w * 16 + (lane & 15);
+    const int c = ks * 2 + (lane >> 4);
+    ldsm_x4(smem_u32(sQ + tile_off<D>(r, c)), qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
+  }
+  float o[D / 8][4];
+#pragma unroll
+  for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+  const float sl2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
+  const int r0 = lane >> 2;            // rows r0 and r0 + 8 of this warp = tokens
+  const int posq[2] = {P.ctx + r0, P.ctx + r0 + 8};
+
+  const int ntiles = (hi - lo + 63) / 64;
+  for (int it = 0; it < ntiles; ++it) {
+    const int buf = it & 1;
+    const int p0 = lo + it * 64;
+    if (it + 1 < ntiles) {
+      load_kv(buf ^ 1, p0 + 64);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    epi_sync();
+    // S = Q K^T (16 x 64)
+    float s[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+#pragma unroll
+      for (int np = 0; np < 4; ++np) {  // pairs of 8-position tiles
+        const int r = np * 16 + (lane & 7) + ((lane >> 4) << 3);
+        const int c = ks * 2 + ((lane >> 3) & 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(smem_u32(sK[buf] + tile_off<D>(r, c)), b0, b1, b2, b3);
+        mma16816(s[2 * np], qa[ks], b0, b1);
+        mma16816(s[2 * np + 1], qa[ks], b2, b3);
+      }
+    }
+    // mask + online softmax
+    float mx[2] = {mrow[0], mrow[1]};
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = p0 + nt * 8 + 2 * (lane & 3) + (e & 1);
+        const int rr = e >> 1;
+        const int pq = posq[rr];
+        const bool vis = j < hi && j <= pq && (P.window == 0 || pq - j < P.window);
+        const float v = vis ? s[nt][e] * sl2 : -INFINITY;
+        s[nt][e] = v;
+        mx[rr] = fmaxf(mx[rr], v);
+      }
+    }
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
+      mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
+    }
+    float alpha[2], base[2];
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      base[rr] = mx[rr] == -INFINITY ? 0.f : mx[rr];
+      alpha[rr] = mrow[rr] == -INFINITY ? 0.f : exp2f(mrow[rr] - base[rr]);
+      if (mx[rr] == -INFINITY) alpha[rr] = 1.f;
+      mrow[rr] = mx[rr];
+      lrow[rr] *= alpha[rr];
+    }
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) {
+      o[i][0] *= alpha[0];
+      o[i][1] *= alpha[0];
+      o[i][2] *= alpha[1];
+      o[i][3] *= alpha[1];
+    }
+    uint32_t pa[4][4];  // P as A fragments, 4 k16 steps over 64 positions
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      const float p0v = exp2f(s[nt][0] - base[0]), p1v = exp2f(s[nt][1] - base[0]);
+      const float p2v = exp2f(s[nt][2] - base[1]), p3v = exp2f(s[nt][3] - base[1]);
+      lrow[0] += p0v + p1v;
+      lrow[1] += p2v + p3v;
+      const int kk = nt >> 1, hi8 = nt & 1;
+      pa[kk][hi8 * 2 + 0] = pack_bf16(p0v, p1v);
+      pa[kk][hi8 * 2 + 1] = pack_bf16(p2v, p3v);
+    }
+    // O += P V
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+      for (int dp = 0; dp < D / 16; ++dp) {  // pairs of 8-wide d tiles
+        const int r = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+        const int c = dp * 2 + (lane >> 4);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(smem_u32(sV[buf] + tile_off<D>(r, c)), b0, b1, b2, b3);
+        mma16816(o[2 * dp], pa[kk], b0, b1);
+        mma16816(o[2 * dp + 1], pa[kk], b2, b3);
+      }
+    }
+    epi_sync();
+  }
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    lrow[rr] += __shfl_xor_sync(0xffffffffu, lrow[rr], 1);
+    lrow[rr] += __shfl_xor_sync(0xffffffffu, lrow[rr], 2);
+  }
+  // partial: [unit][row][D + 2] = o (unnormalised), m, l
+  float* dst = P.attn_part + static_cast<size_t>(g * P.attn_chunks + chunk_id) * 64 * (D + 2);
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    const int row = w * 16 + r0 + 8 * rr;
+    float* pr = dst + static_cast<size_t>(row) * (D + 2);
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) {
+      const int col = i * 8 + 2 * (lane & 3);
+      *reinterpret_cast<float2*>(pr + col) = make_float2(o[i][2 * rr], o[i][2 * rr + 1]);
+    }
+    if ((lane & 3) == 0) {
+      pr[D] = mrow[rr];
+      pr[D + 1] = lrow[rr];
+    }
+  }
+}
+
+// Merge of the attention partials of one (token, q head): o = sum_c 2^(m_c-M) o_c / L.
+template <int D>
+MK_DEV void merge_item(const LayerParams& P, int item, int et) {
+  const int t = item / P.Hq, hq = item % P.Hq;
+  const int g = hq / 4, hl = hq % 4;
+  const int row = hl * 16 + t;
+  const size_t stride = static_cast<size_t>(64) * (D + 2);
+  const float* base = P.attn_part + static_cast<size_t>(g * P.attn_chunks) * stride +
+                      static_cast<size_t>(row) * (D + 2);
+  float M = -INFINITY;
+  for (int c = 0; c < P.attn_chunks; ++c) M = fmaxf(M, base[c * stride + D]);
+  if (et >= D) return;
+  float L = 0.f, acc = 0.f;
+  for (int c = 0; c < P.attn_chunks; ++c) {
+    const float* pc = base + c * stride;
+    const float mc = pc[D];
+    if (mc == -INFINITY) continue;
+    const float wgt = exp2f(mc - M);
+    L += wgt * pc[D + 1];
+    acc += wgt * pc[et];
+  }
+  P.o_buf[static_cast<size_t>(t) * P.Hq * D + hq * D + et] = to_bf(acc / L);
+}
+
+MK_DEV bool epi_arrive(const LayerParams& P, const Smem& S, int id, int et) {
+  __threadfence();
+  epi_sync();
+  if (et == 0) red_release_add(P.bar_ctr + id, 1u);
+  return true;
+}
+
+MK_DEV bool epi_wait(const LayerParams& P, const Smem& S, int id, uint32_t target, int et) {
+  if (et == 0 && !grid_wait(P, S, id, target)) atomicExch(&S.m->abort, 1u);
+  epi_sync();
+  return !aborted(P, S);
+}
+
+MK_DEV void run_epilogue(const LayerParams& P, const Smem& S, uint32_t epoch) {
+  Misc* m = S.m;
+  const int et = threadIdx.x - 128;  // 0..127
+  const uint32_t target = grid_target(P, epoch);
+  uint32_t acc_ph[2] = {0, 0}, ucount = 0;
+  bool ok = true;
+  const int last_ph = P.fuse_next ? PH_NQKV : (P.moe ? PH_UNPOOL : PH_DOWN);
+  for (int ph = 0; ph < PH_COUNT && ok; ++ph) {
+    if (!phase_active(P, ph)) continue;
+    if (ph == last_ph && et == 0) pdl_launch_dependents();
+    if (ph == PH_ATTN) {
+      if (P.first_layer && !(ok = epi_wait(P, S, BAR_QKV, target, et))) break;
+      const int n = phase_units(P, S, ph);
+      for (int u = first_unit(P, ph); u < n; u += P.grid) {
+        const int g = u / P.attn_chunks, c = u % P.attn_chunks;
+        const int lo = P.attn_lo + c * P.attn_chunk_len;
+        const int hi = min(P.ctx + P.T, lo + P.attn_chunk_len);
+        if (P.d == 128) attention_unit<128>(P, S, g, lo, hi, c, et);
+        else attention_unit<64>(P, S, g, lo, hi, c, et);
+      }
+      epi_arrive(P, S, BAR_ATTN, et);
+      continue;
+    }
+    if (ph == PH_MERGE) {
+      if (!(ok = epi_wait(P, S, BAR_ATTN, target, et))) break;
+      const int n = phase_units(P, S, ph);
+      for (int u = first_unit(P, ph); u < n; u += P.grid) {
+        if (P.d == 128) merge_item<128>(P, u, et);
+        else merge_item<64>(P, u, et);
+      }
+      epi_arrive(P, S, BAR_MERGE, et);
+      continue;
+    }
+    // GEMM phases: inputs the epilogue itself reads
+    if (ph == PH_GU) {
+      if (!(ok = wait_bar(P, S, &m->route_ready, 0, ERR_TIMEOUT_ROUTE))) break;
+      if (!(ok = epi_wait(P, S, BAR_RP, target, et))) break;
+      if (et < P.T) {
+        float a = 0.f;
+        for (int j = 0; j < P.P / 128; ++j) a = fmaxf(a, P.pamax[j * kMaxT + et]);
+        m->srow_ep[et] = a > 0.f ? __fdiv_rn(a, 2688.0f) : 1.0f;
+      }
+      epi_sync();
+    } else if (ph == PH_DOWN && P.moe) {
+      if (!(ok = epi_wait(P, S, BAR_GU, target, et))) break;
+      for (int s = et; s < P.T * P.topk; s += 128) {
+        float a = 0.f;
+        for (int j = 0; j < P.I / 128; ++j) a = fmaxf(a, P.aamax[s * (P.I / 128) + j]);
+        m->srow_ep[s] = a > 0.f ? __fdiv_rn(a, 2688.0f) : 1.0f;
+      }
+      epi_sync();
+    }
+    const int n = phase_units(P, S, ph);
+    for (int u = first_unit(P, ph); u < n && ok; u += P.grid) {
+      const Unit U = make_unit(P, S, ph, u);
+      const uint32_t b = ucount & 1;
+      ok = epi_gemm_unit(P, S, ph, U, b, acc_ph[b], et);
+      ++ucount;
+    }
+    if (!ok) break;
+    epi_arrive(P, S, phase_arrive(P, ph), et);
+  }
+  // CTA 0 advances the epoch once every CTA has finished this launch.
+  if (ok && blockIdx.x == 0) {
+    if (epi_wait(P, S, final_barrier(P), target, et) && et == 0) {
+      __threadfence();
+      *P.epoch = epoch + 1u;
+    }
+  }
+}
+
+// ============================================================ kernel
+__global__ void __launch_bounds__(kThreads, 1) mk_layer_kernel(const __grid_constant__ LayerParams P) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  Smem S;
+  S.base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                      ~static_cast<uintptr_t>(1023));
+  S.m = reinterpret_cast<Misc*>(S.base + kOffMisc);
+  const int warp = threadIdx.x >> 5;
+  Misc* m = S.m;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&m->full[s], 1);
+      mbar_init(&m->empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&m->bfull[b], 1);
+      mbar_init(&m->bempty[b], 1);
+      mbar_init(&m->accfull[b], 1);
+      mbar_init(&m->accempty[b], 4);
+    }
+    mbar_init(&m->route_ready, 1);
+    mbar_init(&m->mma_done, 1);
+    m->abort = 0;
+    m->n_act = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&m->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  if (warp == 0) {
+    // weights depend on nothing in flight: stream them before the previous
+    // launch has finished
+    if (lane_id() == 0) run_producer(P, S);
+  } else {
+    pdl_wait();
+    // One read of the launch epoch per CTA, before any of its arrivals: CTA 0
+    // advances the epoch only after every CTA has arrived on the last counter.
+    if (threadIdx.x == 32) m->epoch = *reinterpret_cast<volatile uint32_t*>(P.epoch);
+    named_bar(3, kThreads - 32);
+    const uint32_t epoch = m->epoch;
+    if (warp == 1) {
+      if (lane_id() == 0) run_mma(P, S);
+    } else if (warp < 4) {
+      run_stager(P, S, epoch);
+    } else {
+      run_epilogue(P, S, epoch);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(m->tmem_base, kTmemCols);
+  }
+}
+
+const void* layer_kernel_ptr() { return reinterpret_cast<const void*>(&mk_layer_kernel); }
+uint32_t layer_smem_bytes() { return kSmemBytes; }
+
+}  // namespace mk

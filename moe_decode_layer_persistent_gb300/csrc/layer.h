@@ -3,6 +3,7 @@
 #pragma once
 #include <cuda.h>
 #include <cstdint>
+#include <cuda_bf16.h>
 
 namespace mk {
 
@@ -13,7 +14,7 @@ constexpr int kMaxT = 16;         // verify tokens per step (MMA N)
 constexpr int kMaxE = 256;
 constexpr int kMaxK = 8;          // top-k
 constexpr int kTmemCols = 256;
-constexpr int kNumCounters = 8;   // grid-wide dependency counters
+constexpr int kNumCounters = 16;  // grid-wide dependency counters
 
 // Phases of one launch, in order.
 enum PhaseId : int {
@@ -29,10 +30,19 @@ enum PhaseId : int {
   PH_COUNT = 9
 };
 
-// Grid dependency counters (one per dependency stop).
+// Grid dependency counters (one per dependency stop).  Each CTA arrives once
+// per launch on every counter its layer uses; a launch waits for
+// (epoch + 1) * grid arrivals.
 enum BarrierId : int {
-  BAR_QKV = 0, BAR_ATTN = 1, BAR_MERGE = 2, BAR_O = 3, BAR_RP = 4, BAR_GU = 5, BAR_DOWN = 6,
-  BAR_LAST = 7
+  BAR_QKV = 0,    // q and the new K/V rows written
+  BAR_ATTN = 1,   // attention partials written
+  BAR_MERGE = 2,  // o written
+  BAR_O = 3,      // x_mid and its sum-of-squares partials written
+  BAR_RP = 4,     // logits, top-k, p (MoE) | dense SwiGLU output (dense)
+  BAR_GU = 5,     // expert SwiGLU rows and their amax partials written
+  BAR_DOWN = 6,   // z slots and the combined y written
+  BAR_X = 7,      // x_out and its sum-of-squares partials written
+  BAR_END = 8     // next layer's q and K/V rows written
 };
 
 struct LayerParams {

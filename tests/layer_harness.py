@@ -1,0 +1,155 @@
+"""Shared harness of the GPU parity tests: run one layer (or a stack) through
+the C ABI on seeded synthetic inputs, run the oracle on the same inputs, and
+compare with the tolerances of the layer's contract:
+  router expert indices bit-exact;
+  x_out, written K/V rows and next-layer q: max |err| <= 2e-2 * RMS(ref) and
+  cosine >= 0.9995.
+"""
+
+import numpy as np
+import torch
+
+from moe_decode_layer_persistent_gb300 import synth
+import oracle_io as oio
+from oracle import layer as ol
+
+ABS_TOL = 2e-2
+COS_TOL = 0.9995
+
+
+def metrics(got, ref):
+    got = np.asarray(got, dtype=np.float64).ravel()
+    ref = np.asarray(ref, dtype=np.float64).ravel()
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    maxabs = float(np.max(np.abs(got - ref))) if got.size else 0.0
+    den = float(np.linalg.norm(got) * np.linalg.norm(ref))
+    cos = float(np.dot(got, ref) / den) if den > 0 else (1.0 if maxabs == 0 else 0.0)
+    return dict(rms=rms, maxabs=maxabs, rel=maxabs / rms if rms > 0 else maxabs, cos=cos)
+
+
+def assert_close(name, got, ref):
+    m = metrics(got, ref)
+    assert np.all(np.isfinite(np.asarray(got, dtype=np.float64))), name + ": non-finite"
+    assert m["maxabs"] <= ABS_TOL * m["rms"] and m["cos"] >= COS_TOL, "%s: %s" % (name, m)
+    return m
+
+
+def weights_for_lib(W):
+    """The weight dict as the C ABI expects it (device tensors)."""
+    return dict(W)
+
+
+def make_layer(binding, wl, W, flags, max_ctx, next_W=None, window=None, timeout_ns=0):
+    cfg = binding.make_config(wl, flags=flags, max_ctx=max_ctx, window=window,
+                              timeout_ns=timeout_ns)
+    wd = weights_for_lib(W)
+    if next_W is not None:
+        wd["next_attn_norm_w"] = next_W["attn_norm_w"]
+        wd["next_w_qkv"] = next_W["w_qkv"]
+    return binding.mk_layer_create(cfg, wd)
+
+
+def run_single_layer(binding, work, T=None, ctx=None, fuse_next=False, first_layer=True,
+                     q_in=None, renorm=False, stream=None, keep_layer=False):
+    """One mk_decode_step on device tensors of `work` (a synth.make_workload
+    result on cuda).  Returns host copies of every output."""
+    wl = work["wl"]
+    c = work["cfgs"][0]
+    W = work["Ws"][0]
+    T = wl["T"] if T is None else T
+    ctx = wl["ctx"] if ctx is None else ctx
+    kc, vc = (t.clone() for t in work["caches"][0])
+    max_ctx = kc.shape[0]
+    flags = (binding.MK_FIRST_LAYER if first_layer else 0) | \
+        (binding.MK_FUSE_NEXT_QKV if fuse_next else 0) | (binding.MK_TOPK_RENORM if renorm else 0)
+    nxt = work["next"] if fuse_next else None
+    layer = make_layer(binding, c, W, flags, max_ctx, next_W=nxt)
+    x_in = work["x_in"][:T].contiguous()
+    x_out = torch.zeros_like(x_in)
+    dev = x_in.device
+    k = c.get("top_k", 0)
+    idx = torch.full((T, max(k, 1)), -1, dtype=torch.int32, device=dev)
+    wts = torch.zeros((T, max(k, 1)), dtype=torch.float32, device=dev)
+    q_out = nkc = nvc = None
+    if fuse_next:
+        nkc, nvc = (t.clone() for t in (nxt["k_cache"], nxt["v_cache"]))
+        q_out = torch.zeros((T, c["n_q_heads"] * c["head_dim"]), dtype=torch.bfloat16, device=dev)
+    io = binding.make_step_io(T, ctx, x_in, x_out, kc, vc, q_in=q_in, next_k_cache=nkc,
+                              next_v_cache=nvc, q_out=q_out,
+                              topk_idx_out=idx if k else None, topk_w_out=wts if k else None)
+    binding.mk_decode_step(layer, io, stream)
+    torch.cuda.synchronize()
+    st = binding.mk_layer_status(layer)
+    out = dict(status=st, x_out=x_out.cpu(), k_cache=kc.cpu(), v_cache=vc.cpu(),
+               idx=idx.cpu().numpy() if k else None, w=wts.cpu().numpy() if k else None)
+    if fuse_next:
+        out.update(q_out=q_out.cpu(), next_k_cache=nkc.cpu(), next_v_cache=nvc.cpu())
+    if keep_layer:
+        out["layer"] = layer
+    else:
+        binding.mk_layer_destroy(layer)
+    return out
+
+
+def oracle_single_layer(work, T=None, ctx=None, fuse_next=False, Wn=None, renorm=False):
+    wl = work["wl"]
+    c = work["cfgs"][0]
+    T = wl["T"] if T is None else T
+    ctx = wl["ctx"] if ctx is None else ctx
+    Wn = oio.np_weights(work["Ws"][0]) if Wn is None else Wn
+    kc, vc = (oio.np64(t) for t in work["caches"][0])
+    nxt = None
+    nkc = nvc = None
+    if fuse_next:
+        nxt = oio.np_weights({k: v for k, v in work["next"].items() if k in ("attn_norm_w", "w_qkv")})
+        nkc, nvc = oio.np64(work["next"]["k_cache"]), oio.np64(work["next"]["v_cache"])
+    return ol.layer_forward(oio.oracle_cfg(c), Wn, oio.np64(work["x_in"][:T]), kc, vc, ctx,
+                            next_W=nxt, next_k_cache=nkc, next_v_cache=nvc, renorm=renorm)
+
+
+def compare_single(gpu, ref, T, ctx, fuse_next=False, moe=True):
+    """Asserts the contract; returns the metrics of every compared tensor."""
+    res = {}
+    assert gpu["status"] == 0, "device status %d" % gpu["status"]
+    if moe:
+        assert np.array_equal(gpu["idx"], ref["idx"]), (gpu["idx"], ref["idx"])
+    res["x_out"] = assert_close("x_out", gpu["x_out"].double().numpy(), ref["x_out"])
+    res["k_rows"] = assert_close("k_rows", gpu["k_cache"][ctx:ctx + T].double().numpy(),
+                                 ref["k_cache"][ctx:ctx + T])
+    res["v_rows"] = assert_close("v_rows", gpu["v_cache"][ctx:ctx + T].double().numpy(),
+                                 ref["v_cache"][ctx:ctx + T])
+    # rows outside [ctx, ctx+T) untouched
+    assert np.array_equal(gpu["k_cache"][:ctx].double().numpy(), ref["k_cache"][:ctx])
+    if fuse_next:
+        res["q_out"] = assert_close("q_out", gpu["q_out"].double().numpy(),
+                                    ref["q_next"].reshape(T, -1))
+        res["next_k"] = assert_close("next_k", gpu["next_k_cache"][ctx:ctx + T].double().numpy(),
+                                     ref["k_next"])
+        res["next_v"] = assert_close("next_v", gpu["next_v_cache"][ctx:ctx + T].double().numpy(),
+                                     ref["v_next"])
+    return res
+
+
+def to_device(obj, device):
+    if isinstance(obj, torch.Tensor):
+        return obj.to(device)
+    if isinstance(obj, dict):
+        return {k: to_device(v, device) for k, v in obj.items()}
+    if isinstance(obj, (list, tuple)):
+        return type(obj)(to_device(v, device) for v in obj)
+    return obj
+
+
+def prepare(work_name, device, T=None, ctx=None, layers=None, enforce=True, seed=None):
+    """Synthetic workload on `device`; "host" generates on the CPU generator
+    and moves the tensors to the GPU (small workloads: same values as the CPU
+    tests see)."""
+    gen_dev = "cpu" if device == "host" else device
+    work = synth.make_workload(work_name, device=gen_dev, T=T, ctx=ctx, layers=layers, seed=seed)
+    if device == "host":
+        for key in ("Ws", "caches", "x_in", "next"):
+            work[key] = to_device(work[key], "cuda")
+    Wn = None
+    if enforce and work["wl"]["ffn"] == "moe" and work["wl"]["layers"] == 1:
+        Wn, _ = oio.enforce_margin_single(work)
+    return work, Wn
