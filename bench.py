@@ -1,0 +1,430 @@
+"""Benchmark: latency of the persistent decode layer / layer stack on one GPU.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl mk|reference]
+
+Prints ONE JSON line (rank 0).  A step is one decode step of the workload:
+one layer launch (single-layer workloads) or one launch per layer (stacks),
+16 verify tokens.  value = microseconds per step (device time, CUDA events on
+the launching stream, inputs resident in HBM); e2e = the same through the C
+ABI with host buffers (pinned H2D of x_in and D2H of x_out inside the timed
+region).  roofline: algorithmic bytes of one layer launch (dense weights +
+the distinct experts this step routed to + KV read + KV/activation writes)
+over the average launch duration, against the measured HBM copy bandwidth.
+cpu_baseline: the CPU oracle on a bounded sample of the same workload.
+Multi-GPU: replicas only (one independent replica per rank, no collective).
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "µs per decode layer & per step (16-token verify); HBM GB/s vs roofline"
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        self.path = "/tmp/mk_clocks_%d.csv" % os.getpid()
+        q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + q, "--format=csv,noheader,nounits",
+                 "-lms", "20"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[2]), max=float(parts[3]), power=float(parts[4]),
+                                 hw=parts[6], hwt=parts[7], swt=parts[8], pcap=parts[9]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            if r["hw"].lower() == "active":
+                reasons.add("hw_slowdown")
+            if r["hwt"].lower() == "active":
+                reasons.add("hw_thermal_slowdown")
+            if r["swt"].lower() == "active":
+                reasons.add("sw_thermal_slowdown")
+            if r["pcap"].lower() == "active":
+                reasons.add("sw_power_cap")
+        loaded = [r["sm"] for r in rows]
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ workloads
+def algorithmic_bytes(c, T, ctx, n_experts_touched, first, fuse):
+    """Bytes one layer launch must move at least (weights read once, KV read
+    once, new rows and activations written once)."""
+    H, Hq, Hkv, d = c["hidden"], c["n_q_heads"], c["n_kv_heads"], c["head_dim"]
+    nqkv = (Hq + 2 * Hkv) * d
+    b = 2 * H * Hq * d                              # o-proj
+    if first:
+        b += 2 * nqkv * H
+    if fuse:
+        b += 2 * nqkv * H + 2 * T * 2 * Hkv * d     # next QKV + next K/V rows
+    if c["ffn"] == "moe":
+        E, P, I = c["n_experts"], c["pooled_dim"], c["expert_inter"]
+        b += 2 * E * H + 2 * P * H + 2 * H * P       # router, pooler, unpooler
+        per_expert = 2 * (I * P // 2 + I * P // 16) + (P * I // 2 + P * I // 16) + 12
+        b += n_experts_touched * per_expert
+    else:
+        F = c["dense_inter"]
+        b += 2 * 3 * F * H
+    lo = max(0, ctx - c["window"] + 1) if c["window"] else 0
+    b += 2 * 2 * (ctx + T - lo) * Hkv * d           # K and V rows read
+    b += 2 * 2 * T * Hkv * d                        # K and V rows written
+    b += 2 * 2 * T * H + (0 if first else 2 * T * Hq * d)   # x in/out, q in
+    return b
+
+
+def build_layers(B, work):
+    cfgs, Ws = work["cfgs"], work["Ws"]
+    L = len(Ws)
+    max_ctx = work["caches"][0][0].shape[0]
+    layers = []
+    for l in range(L):
+        fuse = l + 1 < L or (L == 1 and work["next"] is not None)
+        flags = (B.MK_FIRST_LAYER if l == 0 else 0) | (B.MK_FUSE_NEXT_QKV if fuse else 0)
+        cfg = B.make_config(cfgs[l], flags=flags, max_ctx=max_ctx)
+        wd = dict(Ws[l])
+        nxt = Ws[l + 1] if l + 1 < L else work["next"]
+        if fuse:
+            wd["next_attn_norm_w"], wd["next_w_qkv"] = nxt["attn_norm_w"], nxt["w_qkv"]
+        layers.append(B.mk_layer_create(cfg, wd))
+    return layers
+
+
+class Runner:
+    """Holds the device state of one replica and runs steps."""
+
+    def __init__(self, B, work, stream):
+        self.B, self.work, self.stream = B, work, stream
+        wl = work["wl"]
+        self.T, self.ctx = wl["T"], wl["ctx"]
+        self.layers = build_layers(B, work)
+        self.L = len(self.layers)
+        self.stack = B.mk_stack_create(self.layers) if self.L > 1 else None
+        self.kcs = [c[0] for c in work["caches"]]
+        self.vcs = [c[1] for c in work["caches"]]
+        self.x_in = work["x_in"].contiguous()
+        self.x_out = torch.zeros_like(self.x_in)
+        k = wl.get("top_k", 0)
+        self.moe = wl["ffn"] == "moe"
+        self.idx = torch.zeros((self.L, self.T, max(k, 1)), dtype=torch.int32, device="cuda")
+        if self.L == 1:
+            nx = work["next"]
+            self.q_out = torch.zeros((self.T, wl["n_q_heads"] * wl["head_dim"]),
+                                     dtype=torch.bfloat16, device="cuda") if nx else None
+            self.io = B.make_step_io(self.T, self.ctx, self.x_in, self.x_out, self.kcs[0], self.vcs[0],
+                                     next_k_cache=nx["k_cache"] if nx else None,
+                                     next_v_cache=nx["v_cache"] if nx else None, q_out=self.q_out,
+                                     topk_idx_out=self.idx[0] if self.moe else None)
+        else:
+            self.io = B.make_stack_io(self.T, self.ctx, self.x_in, self.x_out, self.kcs, self.vcs,
+                                      topk_idx_out=self.idx if self.moe else None)
+
+    @property
+    def launches_per_step(self):
+        return self.L
+
+    def step(self):
+        if self.stack is not None:
+            self.B.mk_stack_step(self.stack, self.io, self.stream)
+        else:
+            self.B.mk_decode_step(self.layers[0], self.io, self.stream)
+
+    def status(self):
+        return self.B.mk_stack_status(self.stack) if self.stack is not None else \
+            self.B.mk_layer_status(self.layers[0])
+
+    def experts_touched(self):
+        if not self.moe:
+            return [0] * self.L
+        idx = self.idx.cpu().numpy()
+        return [len(set(idx[l].ravel().tolist())) for l in range(self.L)]
+
+    def close(self):
+        if self.stack is not None:
+            self.B.mk_stack_destroy(self.stack)
+        for lay in self.layers:
+            self.B.mk_layer_destroy(lay)
+
+
+def cpu_baseline(work, samples_layers):
+    """Oracle wall time on the host cores for a bounded sample: the listed
+    layers of the workload (single tokens of work are not sampled: every
+    sampled layer runs all 16 verify tokens).  Returns seconds per sampled
+    layer, per layer kind."""
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle_io as oio
+    from oracle import layer as ol
+    out = {}
+    for l in samples_layers:
+        c = work["cfgs"][l]
+        Wn = oio.np_weights(work["Ws"][l])
+        kc, vc = (oio.np64(t) for t in work["caches"][l])
+        x = oio.np64(work["x_in"])
+        q = None
+        if l > 0:  # a non-first layer needs q: use the layer's own QKV as the sample input
+            q, kn, vn = ol.qkv_project(x, Wn["attn_norm_w"], Wn["w_qkv"], c["n_q_heads"],
+                                       c["n_kv_heads"], c["head_dim"])
+            ctx = work["wl"]["ctx"]
+            kc[ctx:ctx + x.shape[0]], vc[ctx:ctx + x.shape[0]] = kn, vn
+        t0 = time.perf_counter()
+        ol.layer_forward(oio.oracle_cfg(c), Wn, x, kc, vc, work["wl"]["ctx"], q_in=q,
+                         first_layer=(l == 0))
+        out[l] = time.perf_counter() - t0
+    return out
+
+
+def host_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="swa_layer")
+    ap.add_argument("--impl", default="mk", choices=["mk", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl == "mk" else "gloo")
+    from moe_decode_layer_persistent_gb300 import synth
+
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    torch.cuda.set_device(local_rank)
+    from moe_decode_layer_persistent_gb300 import binding as B
+    # each replica draws its own inputs (seed offset by rank)
+    work = synth.make_workload(args.workload, device="cuda",
+                               seed=synth.SEED_BASE + synth.WORKLOADS[args.workload]["index"] + 1000 * rank)
+    stream = torch.cuda.Stream()
+    R = Runner(B, work, stream)
+    wl = work["wl"]
+    single = R.L == 1
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda") if single else None
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            if flush is not None:
+                flush.fill_(1.0)
+            R.step()
+    torch.cuda.synchronize()
+    st = R.status()
+    if st != 0:
+        raise RuntimeError("device status %s after warm-up" % B.mk_status_string(st))
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.2)
+    # timed region: K steps; single-layer workloads flush L2 between steps
+    # (outside the per-step events); stacks read >> L2 per step.
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            if flush is not None:
+                flush.fill_(float(i))
+            evs[i][0].record(stream)
+            R.step()
+            evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    if world > 1:
+        torch.distributed.barrier()
+    ms = [a.elapsed_time(b) for a, b in evs]
+    ms_step = sum(ms) / len(ms)
+    # keep the GPU busy a little longer so the sampler sees the load, then stop
+    ck = clocks.stop()
+    st = R.status()
+    if st != 0:
+        raise RuntimeError("device status %s in timed region" % B.mk_status_string(st))
+    if world > 1:
+        t = torch.tensor([ms_step], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+
+    # e2e: host buffers, pinned H2D of x_in and D2H of x_out in every step
+    x_host = work["x_in"].cpu().pin_memory()
+    y_host = torch.empty_like(x_host).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(args.steps):
+            R.x_in.copy_(x_host, non_blocking=True)
+            R.step()
+            y_host.copy_(R.x_out, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    bytes_io = x_host.numel() * x_host.element_size()
+
+    # roofline of the layer kernel (the only kernel of the step)
+    touched = R.experts_touched()
+    first_flags = [l == 0 for l in range(R.L)]
+    fuse_flags = [(l + 1 < R.L) or (R.L == 1 and work["next"] is not None) for l in range(R.L)]
+    alg = [algorithmic_bytes(work["cfgs"][l], R.T, R.ctx, touched[l], first_flags[l], fuse_flags[l])
+           for l in range(R.L)]
+    alg_per_launch = sum(alg) / R.L
+    launch_s = ms_step / 1e3 / R.L
+    peak, peak_kind = load_peaks()
+    achieved = alg_per_launch / launch_s / 1e9
+
+    us_step = ms_step * 1e3
+    line = {
+        "metric": METRIC, "value": round(us_step * (1.0 if world == 1 else 1.0), 3),
+        "unit": "us/step", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 + nvfp4 (fp32 accumulate)", "data": "synthetic",
+        "config": {"workload": args.workload, "layers": R.L, "T": R.T, "ctx": R.ctx,
+                   "hidden": wl["hidden"], "ffn": wl["ffn"],
+                   "l2": "flushed between steps (512 MB write)" if single else
+                         "inputs larger than L2 (%.1f GB read per step)" % (sum(alg) / 1e9),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "us_per_layer": round(us_step / R.L, 3),
+        "experts_touched_mean": round(float(np.mean(touched)), 2) if R.moe else None,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "frac_of_8TBs": round(achieved / 8000.0, 4),
+                     "algorithmic_bytes_per_launch": int(alg_per_launch), "traffic": None},
+        "e2e": {"value": round(e2e_ms * 1e3, 3), "unit": "us/step",
+                "h2d_bytes_per_step": bytes_io, "d2h_bytes_per_step": bytes_io},
+        "gpu_launches": args.steps * R.launches_per_step,
+        "timed_wall_s": round(t_wall, 4),
+        "clocks": ck,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        samples = [0] if R.L == 1 else sorted({0, next(l for l in range(R.L) if work["cfgs"][l]["window"] == 0)})
+        tl = cpu_baseline(work, samples)
+        if R.L == 1:
+            per_step = tl[0]
+            sample = "layer 0 of %s, all %d tokens (the whole step)" % (args.workload, R.T)
+        else:
+            glob = [l for l in range(R.L) if work["cfgs"][l]["window"] == 0]
+            t_g = tl[samples[-1]]
+            t_s = tl[0] if work["cfgs"][0]["window"] else t_g
+            per_step = t_s * (R.L - len(glob)) + t_g * len(glob)
+            sample = ("layers %s of %s (all %d tokens each), scaled to %d layers by window kind"
+                      % (samples, args.workload, R.T, R.L))
+        line["cpu_baseline"] = {"value": round(per_step * 1e6, 1), "unit": "us/step",
+                                "cores": host_threads(), "kind": "oracle", "sample": sample}
+    R.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step is one bounded sample of the
+    workload (one layer launch's work, all 16 tokens), timed on host cores."""
+    if rank != 0:
+        return
+    from moe_decode_layer_persistent_gb300 import synth
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle_io as oio
+    from oracle import layer as ol
+    work = synth.make_workload(args.workload, device="cpu", layers=1)
+    c = work["cfgs"][0]
+    Wn = oio.np_weights(work["Ws"][0])
+    kc, vc = (oio.np64(t) for t in work["caches"][0])
+    x = oio.np64(work["x_in"])
+    nW = None
+    if work["next"] is not None:
+        nW = oio.np_weights({k: work["next"][k] for k in ("attn_norm_w", "w_qkv")})
+        nkc, nvc = oio.np64(work["next"]["k_cache"]), oio.np64(work["next"]["v_cache"])
+    else:
+        nkc = nvc = None
+
+    def one():
+        ol.layer_forward(oio.oracle_cfg(c), Wn, x, kc, vc, work["wl"]["ctx"], next_W=nW,
+                         next_k_cache=nkc, next_v_cache=nvc)
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    dt = (time.perf_counter() - t0) / args.steps
+    L = synth.WORKLOADS[args.workload]["layers"]
+    us = dt * 1e6 * L
+    line = {"metric": METRIC, "value": round(us, 1), "unit": "us/step", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 3),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": args.workload, "layers": L, "T": work["wl"]["T"],
+                       "ctx": work["wl"]["ctx"]},
+            "cpu_baseline": {"value": round(us, 1), "unit": "us/step", "cores": host_threads(),
+                             "kind": "oracle",
+                             "sample": "one layer of %s per step (all tokens), x%d layers"
+                                       % (args.workload, L)},
+            "e2e": {"value": round(us, 1), "unit": "us/step", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

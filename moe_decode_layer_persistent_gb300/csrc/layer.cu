@@ -1090,7 +1090,10 @@ MK_DEV void attention_unit(const LayerParams& P, const Smem& S, int g, int lo, i
       o[i][2] *= alpha[1];
       o[i][3] *= alpha[1];
     }
-    uint32_t pa[4][4];  // P as A fragments, 4 k16 steps over 64 positions
+    // P as A fragments (4 k16 steps over 64 positions), split into a bf16
+    // high part and the bf16 rounding of the remainder, so that P V is
+    // accumulated from a ~16-bit-mantissa P rather than bf16's 8 bits.
+    uint32_t pa[4][4], pl[4][4];
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
       const float p0v = exp2f(s[nt][0] - base[0]), p1v = exp2f(s[nt][1] - base[0]);
@@ -1098,8 +1101,11 @@ MK_DEV void attention_unit(const LayerParams& P, const Smem& S, int g, int lo, i
       lrow[0] += p0v + p1v;
       lrow[1] += p2v + p3v;
       const int kk = nt >> 1, hi8 = nt & 1;
-      pa[kk][hi8 * 2 + 0] = pack_bf16(p0v, p1v);
-      pa[kk][hi8 * 2 + 1] = pack_bf16(p2v, p3v);
+      const float h0 = round_bf(p0v), h1 = round_bf(p1v), h2 = round_bf(p2v), h3 = round_bf(p3v);
+      pa[kk][hi8 * 2 + 0] = pack_bf16(h0, h1);
+      pa[kk][hi8 * 2 + 1] = pack_bf16(h2, h3);
+      pl[kk][hi8 * 2 + 0] = pack_bf16(p0v - h0, p1v - h1);
+      pl[kk][hi8 * 2 + 1] = pack_bf16(p2v - h2, p3v - h3);
     }
     // O += P V
 #pragma unroll
@@ -1112,6 +1118,8 @@ MK_DEV void attention_unit(const LayerParams& P, const Smem& S, int g, int lo, i
         ldsm_x4_t(smem_u32(sV[buf] + tile_off<D>(r, c)), b0, b1, b2, b3);
         mma16816(o[2 * dp], pa[kk], b0, b1);
         mma16816(o[2 * dp + 1], pa[kk], b2, b3);
+        mma16816(o[2 * dp], pl[kk], b0, b1);
+        mma16816(o[2 * dp + 1], pl[kk], b2, b3);
       }
     }
     epi_sync();

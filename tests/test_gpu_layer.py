@@ -1,0 +1,227 @@
+"""GPU parity of the persistent decode layer against the oracle (all through
+the C ABI), on seeded synthetic inputs of the five workloads and of ragged
+and edge-case sizes."""
+
+import numpy as np
+import pytest
+import torch
+
+from moe_decode_layer_persistent_gb300 import synth
+import layer_harness as H
+import oracle_io as oio
+from oracle import layer as ol
+
+pytestmark = pytest.mark.gpu
+
+
+def _single(binding, name, dev, T=None, ctx=None, fuse=False, renorm=False, **kw):
+    work, Wn = H.prepare(name, dev, T=T, ctx=ctx, **kw)
+    g = H.run_single_layer(binding, work, fuse_next=fuse, renorm=renorm)
+    r = H.oracle_single_layer(work, fuse_next=fuse, Wn=Wn, renorm=renorm)
+    wl = work["wl"]
+    res = H.compare_single(g, r, wl["T"], wl["ctx"], fuse_next=fuse, moe=wl["ffn"] == "moe")
+    if wl["ffn"] == "moe":
+        assert np.allclose(g["w"], r["w"], rtol=1e-5, atol=1e-7)
+    return res
+
+
+def test_tiny_layer(cuda_lib):
+    """1 token, 128 past positions, 16 experts top-2, head_dim 64."""
+    _single(cuda_lib, "tiny_layer", "host")
+
+
+@pytest.mark.parametrize("T,ctx", [(16, 100), (3, 0), (5, 1), (16, 128), (7, 257)])
+def test_tiny_shapes_ragged(cuda_lib, T, ctx):
+    _single(cuda_lib, "tiny_layer", "host", T=T, ctx=ctx)
+
+
+def test_tiny_renormalised_topk(cuda_lib):
+    _single(cuda_lib, "tiny_layer", "host", T=4, ctx=50, renorm=True)
+
+
+def test_swa_layer(cuda_lib):
+    """16 verify tokens, context 8192, window 2048, 256 experts top-8."""
+    _single(cuda_lib, "swa_layer", "cuda")
+
+
+def test_swa_layer_short_context_equals_global(cuda_lib):
+    """ctx + T <= window: the sliding-window layer equals the global one."""
+    work, Wn = H.prepare("swa_layer", "cuda", ctx=2000)
+    g_swa = H.run_single_layer(cuda_lib, work)
+    work["cfgs"][0] = dict(work["cfgs"][0], window=0)
+    g_glob = H.run_single_layer(cuda_lib, work)
+    assert torch.equal(g_swa["x_out"], g_glob["x_out"])
+
+
+def test_global_layer_fused_next_qkv(cuda_lib):
+    """Context 32768, global attention, fused next-layer QKV + KV write."""
+    _single(cuda_lib, "global_layer_fused", "cuda", fuse=True)
+
+
+def test_dense_layer(cuda_lib):
+    _single(cuda_lib, "dense_draft_stack", "cuda", layers=1)
+
+
+def test_repeated_steps_and_determinism(cuda_lib):
+    work, Wn = H.prepare("tiny_layer", "host", T=16, ctx=60)
+    c = work["cfgs"][0]
+    kc, vc = (t.clone() for t in work["caches"][0])
+    layer = H.make_layer(cuda_lib, c, work["Ws"][0], cuda_lib.MK_FIRST_LAYER, kc.shape[0])
+    outs = []
+    for _ in range(3):
+        x_out = torch.zeros_like(work["x_in"])
+        io = cuda_lib.make_step_io(16, 60, work["x_in"], x_out, kc, vc)
+        cuda_lib.mk_decode_step(layer, io)
+        torch.cuda.synchronize()
+        outs.append(x_out.clone())
+    assert cuda_lib.mk_layer_status(layer) == 0
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+    cuda_lib.mk_layer_destroy(layer)
+
+
+def test_bounded_wait_reports_timeout_and_recovers(cuda_lib):
+    """A wait limit of 1 ns makes the first wait that is not already satisfied
+    give up: the kernel returns, the status reads MK_ERR_TIMEOUT, the context
+    stays usable, and after clearing the status the layer runs normally."""
+    work, Wn = H.prepare("tiny_layer", "host", T=4, ctx=30)
+    c = work["cfgs"][0]
+    kc, vc = (t.clone() for t in work["caches"][0])
+    layer = H.make_layer(cuda_lib, c, work["Ws"][0], cuda_lib.MK_FIRST_LAYER, kc.shape[0],
+                         timeout_ns=1)
+    x_out = torch.zeros_like(work["x_in"])
+    io = cuda_lib.make_step_io(4, 30, work["x_in"], x_out, kc, vc)
+    cuda_lib.mk_decode_step(layer, io)
+    torch.cuda.synchronize()
+    assert cuda_lib.mk_layer_status(layer) == 5
+    cuda_lib.mk_layer_destroy(layer)
+    g = H.run_single_layer(cuda_lib, work)
+    r = H.oracle_single_layer(work, Wn=Wn)
+    H.compare_single(g, r, 4, 30)
+
+
+# ------------------------------------------------------------------ stacks
+
+def _stack_gpu(binding, work, T, ctx):
+    cfgs, Ws = work["cfgs"], work["Ws"]
+    L = len(Ws)
+    layers = []
+    max_ctx = work["caches"][0][0].shape[0]
+    for l in range(L):
+        flags = (binding.MK_FIRST_LAYER if l == 0 else 0) | (binding.MK_FUSE_NEXT_QKV if l + 1 < L else 0)
+        layers.append(H.make_layer(binding, cfgs[l], Ws[l], flags, max_ctx,
+                                   next_W=Ws[l + 1] if l + 1 < L else None))
+    stack = binding.mk_stack_create(layers)
+    kcs = [c[0].clone() for c in work["caches"]]
+    vcs = [c[1].clone() for c in work["caches"]]
+    x_in = work["x_in"][:T].contiguous()
+    x_out = torch.zeros_like(x_in)
+    moe = work["wl"]["ffn"] == "moe"
+    k = work["wl"].get("top_k", 1)
+    idx = torch.full((L, T, k), -1, dtype=torch.int32, device="cuda") if moe else None
+    io = binding.make_stack_io(T, ctx, x_in, x_out, kcs, vcs, topk_idx_out=idx)
+    binding.mk_stack_step(stack, io)
+    torch.cuda.synchronize()
+    st = binding.mk_stack_status(stack)
+    binding.mk_stack_destroy(stack)
+    for lay in layers:
+        binding.mk_layer_destroy(lay)
+    return dict(status=st, x_out=x_out.cpu(), k=[t.cpu() for t in kcs], v=[t.cpu() for t in vcs],
+                idx=idx.cpu().numpy() if moe else None)
+
+
+def _router_input(cfg, W, x, kc, vc, ctx, q, first):
+    """h of one layer (the attention half of the oracle layer)."""
+    from oracle.numerics import bf16_round
+    T = x.shape[0]
+    kc, vc = kc.copy(), vc.copy()
+    if first:
+        q, kn, vn = ol.qkv_project(x, W["attn_norm_w"], W["w_qkv"], cfg["n_q_heads"],
+                                   cfg["n_kv_heads"], cfg["head_dim"])
+        kc[ctx:ctx + T], vc[ctx:ctx + T] = kn, vn
+    q = np.asarray(q).reshape(T, cfg["n_q_heads"], cfg["head_dim"])
+    o = bf16_round(ol.attention(q, kc, vc, ctx, cfg["window"])).reshape(T, -1)
+    x_mid = bf16_round(x + o @ W["w_o"].T)
+    return bf16_round(ol.rmsnorm(x_mid, W["ffn_norm_w"]))
+
+
+def _stack_oracle(work, T, ctx, enforce_margin):
+    """The oracle stack, redrawing each MoE layer's router (in layer order)
+    until the k-th/(k+1)-th logit gap is >= 1e-2 for every token."""
+    cfgs = [oio.oracle_cfg(c) for c in work["cfgs"]]
+    Ws = work["Ws"]
+    L = len(Ws)
+    Wn = [oio.np_weights(W) for W in Ws]
+    x = oio.np64(work["x_in"][:T])
+    kcs = [oio.np64(c[0]) for c in work["caches"]]
+    vcs = [oio.np64(c[1]) for c in work["caches"]]
+    q = None
+    per = []
+    for l in range(L):
+        nxt = Wn[l + 1] if l + 1 < L else None
+        if enforce_margin and cfgs[l]["ffn"] == "moe":
+            h = _router_input(cfgs[l], Wn[l], x, kcs[l], vcs[l], ctx, q, l == 0)
+            for draw in range(400):
+                wr = synth.router_weight(work["wl"], work["seed"], l, draw, Ws[l]["w_router"].device)
+                logits, _, _ = ol.router(h, oio.np64(wr), cfgs[l]["top_k"])
+                if np.all(oio.router_margin(logits, cfgs[l]["top_k"]) >= oio.MARGIN):
+                    Ws[l]["w_router"] = wr
+                    Wn[l]["w_router"] = oio.np64(wr)
+                    break
+            else:
+                raise RuntimeError("no router draw met the margin")
+        r = ol.layer_forward(cfgs[l], Wn[l], x, kcs[l], vcs[l], ctx, q_in=q,
+                             first_layer=(l == 0), next_W=nxt,
+                             next_k_cache=kcs[l + 1] if nxt else None,
+                             next_v_cache=vcs[l + 1] if nxt else None)
+        kcs[l], vcs[l] = r["k_cache"], r["v_cache"]
+        if nxt is not None:
+            kcs[l + 1], vcs[l + 1] = r["next_k_cache"], r["next_v_cache"]
+            q = r["q_next"]
+        x = r["x_out"]
+        per.append(r.get("idx"))
+    return dict(x_out=x, k=kcs, v=vcs, idx=per)
+
+
+def _check_stack(g, r, T, ctx, moe):
+    assert g["status"] == 0
+    L = len(r["k"])
+    if moe:
+        for l in range(L):
+            assert np.array_equal(g["idx"][l], r["idx"][l]), "layer %d router" % l
+    H.assert_close("x_out", g["x_out"].double().numpy(), r["x_out"])
+    for l in range(L):
+        H.assert_close("k rows layer %d" % l, g["k"][l][ctx:ctx + T].double().numpy(),
+                       r["k"][l][ctx:ctx + T])
+        H.assert_close("v rows layer %d" % l, g["v"][l][ctx:ctx + T].double().numpy(),
+                       r["v"][l][ctx:ctx + T])
+
+
+def test_dense_draft_stack(cuda_lib):
+    """5 dense GQA layers chained with programmatic dependent launch."""
+    work = synth.make_workload("dense_draft_stack", device="cuda")
+    T, ctx = work["wl"]["T"], work["wl"]["ctx"]
+    r = _stack_oracle(work, T, ctx, enforce_margin=False)
+    g = _stack_gpu(cuda_lib, work, T, ctx)
+    _check_stack(g, r, T, ctx, moe=False)
+
+
+def test_moe_stack_first_layers(cuda_lib):
+    """The first 4 layers of the 62-layer MoE stack (3 sliding-window, 1
+    global), context 16384, PDL-chained, router margin enforced per layer."""
+    work = synth.make_workload("moe_stack", device="cuda", layers=4)
+    T, ctx = work["wl"]["T"], work["wl"]["ctx"]
+    r = _stack_oracle(work, T, ctx, enforce_margin=True)
+    g = _stack_gpu(cuda_lib, work, T, ctx)
+    _check_stack(g, r, T, ctx, moe=True)
+
+
+def test_tiny_stack_mixed_windows(cuda_lib):
+    wl = dict(synth.WORKLOADS["tiny_layer"], layers=3, T=8, ctx=90)
+    work = synth.make_workload(wl, device="cpu")
+    for l, win in enumerate((32, 0, 16)):
+        work["cfgs"][l] = dict(work["cfgs"][l], window=win)
+    for key in ("Ws", "caches", "x_in"):
+        work[key] = H.to_device(work[key], "cuda")
+    r = _stack_oracle(work, 8, 90, enforce_margin=True)
+    g = _stack_gpu(cuda_lib, work, 8, 90)
+    _check_stack(g, r, 8, 90, moe=True)
