@@ -198,6 +198,18 @@ typedef struct mk_layer_info {
 } mk_layer_info;
 mk_status mk_layer_get_info(mk_layer* layer, mk_layer_info* info);
 
+/* Self-timing (page "Muse Spark Open: 1,109 Tokens a Second ...", section
+ * "What the 5.9 ms is still spent on": the kernel times itself with
+ * %globaltimer stamps written by one lane per block).  Enabled for layers
+ * created while the environment holds MK_TIMESTAMPS=1 (else this returns
+ * MK_ERR_UNSUPPORTED).  Copies min(n, grid * 40) stamps of the layer's last
+ * step to host memory: per CTA, 10 rows of 4 u64 -- rows 0..8 are the phases
+ * (QKV, attention, merge, o-proj, router+pool, expert gate/up, expert down,
+ * unpool, next QKV) with (epilogue start, epilogue end, last MMA issued, last
+ * weight tile issued); row 9 is (kernel start, inputs ready, kernel end, 0).
+ * Unused phases read 0.  Synchronous. */
+mk_status mk_get_timestamps(mk_layer* layer, uint64_t* host_buf, size_t n);
+
 #ifdef __cplusplus
 }
 #endif

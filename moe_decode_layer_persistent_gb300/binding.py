@@ -103,9 +103,11 @@ _lib_mk_selftest_mma = _sig("mk_selftest_mma", _c.c_int,
 _lib_mk_selftest_copy_scratch = _sig("mk_selftest_copy_scratch", _c.c_int,
                                      [_vp, _c.c_int32, _vp, _c.c_size_t])
 
+_lib_mk_get_timestamps = _sig("mk_get_timestamps", _c.c_int, [_vp, _c.c_void_p, _c.c_size_t])
+
 EXPORTED = ["mk_layer_create", "mk_decode_step", "mk_layer_status", "mk_layer_clear_status",
             "mk_layer_destroy", "mk_stack_create", "mk_stack_step", "mk_stack_status",
-            "mk_stack_destroy", "mk_status_string", "mk_layer_get_info",
+            "mk_stack_destroy", "mk_status_string", "mk_layer_get_info", "mk_get_timestamps",
             "mk_selftest_quantize", "mk_selftest_mma", "mk_selftest_copy_scratch"]
 
 
@@ -251,3 +253,11 @@ def mk_selftest_copy_scratch(layer, which, dst):
     w = SCRATCH[which] if isinstance(which, str) else which
     nbytes = dst.numel() * dst.element_size()
     _check("mk_selftest_copy_scratch", _lib_mk_selftest_copy_scratch(layer, w, _ptr(dst), nbytes))
+
+
+def mk_get_timestamps(layer, grid):
+    """Self-timing stamps of the layer's last step: uint64 array [grid, 10, 4]."""
+    import numpy as np
+    buf = np.zeros((grid, 10, 4), dtype=np.uint64)
+    _check("mk_get_timestamps", _lib_mk_get_timestamps(layer, buf.ctypes.data, buf.size))
+    return buf

@@ -2,6 +2,7 @@
 // descriptors and the launches of the persistent layer kernel (one launch per
 // layer; a stack chains them with programmatic dependent launch).
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -348,6 +349,10 @@ mk_status mk_layer_create(const mk_layer_config* cfg, const mk_layer_weights* w,
   MK_TRY(dalloc(L, &P.bar_ctr, kNumCounters));
   MK_TRY(dalloc(L, &P.epoch, 1));
   MK_TRY(dalloc(L, &P.status, 1));
+  {
+    const char* e = std::getenv("MK_TIMESTAMPS");
+    if (e && e[0] == '1') MK_TRY(dalloc(L, &P.ts, static_cast<size_t>(P.grid) * kTsPerCta));
+  }
   if (log_enabled())
     std::fprintf(stderr,
                  "mk: layer grid=%d threads=%d smem=%u tmem=%d scratch=%lld B ffn=%s flags=%u\n",
@@ -476,6 +481,15 @@ mk_status mk_stack_status(mk_stack* S) {
     mk_status s = mk_layer_status(L);
     if (s != MK_OK) return s;
   }
+  return MK_OK;
+}
+
+mk_status mk_get_timestamps(mk_layer* layer, uint64_t* host_buf, size_t n) {
+  if (!layer || !host_buf) return MK_ERR_INVALID_ARG;
+  const LayerParams& P = layer->tmpl;
+  if (!P.ts) return MK_ERR_UNSUPPORTED;
+  const size_t cap = static_cast<size_t>(P.grid) * kTsPerCta;
+  MK_CUDA_TRY(cudaMemcpy(host_buf, P.ts, std::min(n, cap) * sizeof(uint64_t), cudaMemcpyDeviceToHost));
   return MK_OK;
 }
 

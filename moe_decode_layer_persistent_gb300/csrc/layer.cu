@@ -36,6 +36,8 @@ constexpr uint32_t kOffSF = kOffA + kStages * kTileBytes;
 constexpr uint32_t kOffB = kOffSF + kStages * kSfBytes;       // 2 operand buffers
 constexpr uint32_t kBBufBytes = 40960;
 constexpr uint32_t kBSfOff = 16384;                          // scales inside a B buffer
+constexpr uint32_t kLandOff = 16384;   // bf16 units: raw input rows (<= 16 KB), then the gain slice
+constexpr uint32_t kFp4LandOff = 32768; // NVFP4 units: two 4 KB row slots, one per stager warp
 constexpr uint32_t kOffMisc = kOffB + 2 * kBBufBytes;
 constexpr uint32_t kSmemBytes = kOffMisc + 8192 + 1024;     // + alignment slack
 
@@ -48,6 +50,7 @@ struct Misc {
   uint64_t accempty[2];
   uint64_t route_ready;
   uint64_t mma_done;
+  uint64_t land[3];                // stager landing copies: [0] bf16 rows, [1..2] per-warp rows
   uint32_t tmem_base;
   uint32_t abort;
   uint32_t epoch;
@@ -106,6 +109,10 @@ MK_DEV bool wait_bar(const LayerParams& P, const Smem& S, uint64_t* bar, uint32_
   return true;
 }
 
+MK_DEV void stamp(const LayerParams& P, int ph, int slot) {
+  if (P.ts) P.ts[(static_cast<size_t>(blockIdx.x) * (PH_COUNT + 1) + ph) * 4 + slot] = globaltimer();
+}
+
 MK_DEV uint32_t grid_target(const LayerParams& P, uint32_t epoch) {
   return (epoch + 1u) * static_cast<uint32_t>(P.grid);
 }
@@ -134,6 +141,11 @@ MK_DEV void stage_sync() { named_bar(kBarStage, 64); }
 
 // ------------------------------------------------------------ bf16 helpers
 MK_DEV float bf(const __nv_bfloat16 v) { return __bfloat162float(v); }
+// Loads of data other CTAs wrote during this launch go to L2 (never L1, which
+// is not coherent across SMs).
+MK_DEV float ld_bf(const __nv_bfloat16* p) {
+  return __uint_as_float(static_cast<uint32_t>(__ldcg(reinterpret_cast<const unsigned short*>(p))) << 16);
+}
 MK_DEV __nv_bfloat16 to_bf(float v) { return __float2bfloat16_rn(v); }
 MK_DEV float round_bf(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
 MK_DEV float silu(float x) { return x / (1.0f + expf(-x)); }
@@ -324,7 +336,7 @@ MK_DEV void build_routing(const LayerParams& P, const Smem& S) {
   const int nslot = P.T * P.topk;
   for (int s0 = 0; s0 < nslot; s0 += 32) {
     const int s = s0 + lane;
-    const int e = s < nslot ? P.idx[s] : -1 - lane;
+    const int e = s < nslot ? __ldcg(P.idx + s) : -1 - lane;
     const uint32_t peers = __match_any_sync(0xffffffffu, e);
     if (s < nslot && (peers & ((1u << lane) - 1)) == 0) m->cnt[e] += __popc(peers);
     __syncwarp();
@@ -358,7 +370,7 @@ MK_DEV void build_routing(const LayerParams& P, const Smem& S) {
   __syncwarp();
   for (int s0 = 0; s0 < nslot; s0 += 32) {
     const int s = s0 + lane;
-    const int e = s < nslot ? P.idx[s] : -1 - lane;
+    const int e = s < nslot ? __ldcg(P.idx + s) : -1 - lane;
     const uint32_t peers = __match_any_sync(0xffffffffu, e);
     if (s < nslot) {
       const int rank = __popc(peers & ((1u << lane) - 1));
@@ -398,6 +410,7 @@ MK_DEV void run_producer(const LayerParams& P, const Smem& S) {
         }
       }
     }
+    stamp(P, ph, 3);
   }
   // Drain: every issued copy must land before the CTA may exit.
   for (int s = 0; s < kStages; ++s) {
@@ -469,6 +482,7 @@ MK_DEV void run_mma(const LayerParams& P, const Smem& S) {
       b_ph[b] ^= 1;
       ++ucount;
     }
+    stamp(P, ph, 2);
   }
   // all issued tensor-core work completes before TMEM is released
   mma_commit(&m->mma_done);
@@ -479,20 +493,34 @@ MK_DEV void run_mma(const LayerParams& P, const Smem& S) {
 }
 
 // ============================================================ stagers (warps 2-3)
-// Token operand of a bf16 unit: rows t < T of src[t][k0 .. k0 + 64*nkb),
-// optionally x * rnorm[t] * gain[k] rounded to bf16; rows >= T are zero.
-MK_DEV void stage_bf16(const LayerParams& P, const Smem& S, uint8_t* bb, const __nv_bfloat16* src,
-                       int ld, int k0, int nkb, const __nv_bfloat16* gain) {
+// Token operand of a bf16 unit.  The stager leader bulk-copies rows t < T of
+// src[t][k0 .. k0 + 64*nkb) (and the gain slice) into the landing area of the
+// operand buffer; then all stager threads write the swizzled operand, as
+// bf16(x * rnorm[t] * gain[k]) when a gain is given.  Rows >= T are zero.
+MK_DEV bool stage_bf16(const LayerParams& P, const Smem& S, uint8_t* bb, const __nv_bfloat16* src,
+                       int ld, int k0, int nkb, const __nv_bfloat16* gain, uint32_t& land_ph) {
   const int tid = threadIdx.x - 64;
+  uint8_t* raw = bb + kLandOff;
+  uint8_t* graw = raw + kMaxT * nkb * 128;
+  const uint32_t rowbytes = static_cast<uint32_t>(nkb) * 128u;
+  if (tid == 0) {
+    const uint64_t pol = policy_evict_last();
+    mbar_arrive_expect_tx(&S.m->land[0], P.T * rowbytes + (gain ? rowbytes : 0u));
+    for (int t = 0; t < P.T; ++t)
+      bulk_load(raw + t * rowbytes, src + static_cast<size_t>(t) * ld + k0, rowbytes, &S.m->land[0],
+                pol);
+    if (gain) bulk_load(graw, gain + k0, rowbytes, &S.m->land[0], pol);
+  }
+  if (!wait_bar(P, S, &S.m->land[0], land_ph, ERR_TIMEOUT_B)) return false;
+  land_ph ^= 1;
   const int chunks = nkb * 8;  // 16-byte chunks per row
   for (int i = tid; i < kMaxT * chunks; i += 64) {
     const int t = i / chunks, c = i % chunks;
     uint4 v = make_uint4(0, 0, 0, 0);
     if (t < P.T) {
-      const int k = k0 + c * 8;
-      v = *reinterpret_cast<const uint4*>(src + static_cast<size_t>(t) * ld + k);
+      v = *reinterpret_cast<const uint4*>(raw + t * rowbytes + c * 16);
       if (gain) {
-        const uint4 g = *reinterpret_cast<const uint4*>(gain + k);
+        const uint4 g = *reinterpret_cast<const uint4*>(graw + c * 16);
         const float r = S.m->rnorm[t];
         uint32_t* pv = reinterpret_cast<uint32_t*>(&v);
         const uint32_t* pg = reinterpret_cast<const uint32_t*>(&g);
@@ -508,6 +536,7 @@ MK_DEV void stage_bf16(const LayerParams& P, const Smem& S, uint8_t* bb, const _
     const int byte = c * 16;
     *reinterpret_cast<uint4*>(bb + (byte >> 7) * 2048 + sw128_offset(t, byte & 127)) = v;
   }
+  return true;
 }
 
 // Quantiser sink with a given row scale.
@@ -537,8 +566,10 @@ MK_DEV void quantize_row_given_srow(const __nv_bfloat16* row, int K, float s_row
 }
 
 // Token operand of an NVFP4 expert unit: row i = the i-th slot routed to the
-// expert, quantised from bf16 rows of `src` (ld elements apart).
-MK_DEV void stage_fp4(const LayerParams& P, const Smem& S, uint8_t* bb, const Unit& U, bool gu) {
+// expert, quantised from its bf16 row (p for gate/up, the SwiGLU output for
+// down), which each stager warp first bulk-copies into its own landing slot.
+MK_DEV bool stage_fp4(const LayerParams& P, const Smem& S, uint8_t* bb, const Unit& U, bool gu,
+                      uint32_t (&land_ph)[3]) {
   Misc* m = S.m;
   const int warp = (threadIdx.x >> 5) - 2;  // 0..1
   const int e = U.expert;
@@ -555,14 +586,27 @@ MK_DEV void stage_fp4(const LayerParams& P, const Smem& S, uint8_t* bb, const Un
     for (int i = tid; i < 512 * (4 - (K % 256) / 64); i += 64)
       bb[kBSfOff + (kb * 4 + (K % 256) / 64) * 512 + i] = 0;
   }
+  uint8_t* slot = bb + kFp4LandOff + warp * 4096;
+  uint64_t* lb = &m->land[1 + warp];
+  const uint32_t rowbytes = static_cast<uint32_t>(K) * 2u;
   for (int i = warp; i < n; i += 2) {
     const int s = m->slots[m->off[e] + i];
     const int t = s / P.topk;
     const __nv_bfloat16* row = gu ? P.p_buf + static_cast<size_t>(t) * P.P
                                   : P.a_buf + static_cast<size_t>(s) * P.I;
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane_id() == 0) {
+      mbar_arrive_expect_tx(lb, rowbytes);
+      bulk_load(slot, row, rowbytes, lb, policy_evict_last());
+    }
+    if (!wait_bar(P, S, lb, land_ph[1 + warp], ERR_TIMEOUT_B)) return false;
+    land_ph[1 + warp] ^= 1;
     OperandSink sink{bb, bb + kBSfOff, static_cast<uint32_t>(i)};
-    quantize_row_given_srow(row, K, gu ? m->srow_st[t] : m->srow_st[s], sink);
+    quantize_row_given_srow(reinterpret_cast<const __nv_bfloat16*>(slot), K,
+                            gu ? m->srow_st[t] : m->srow_st[s], sink);
   }
+  return true;
 }
 
 MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
@@ -570,7 +614,7 @@ MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
   const int tid = threadIdx.x - 64;  // 0..63
   const int warp = tid >> 5;
   const uint32_t target = grid_target(P, epoch);
-  uint32_t b_ph[2] = {0, 0}, ucount = 0;
+  uint32_t b_ph[2] = {0, 0}, ucount = 0, land_ph[3] = {0, 0, 0};
   bool ok = true;
   // RMSNorm factors of x_in (first layer)
   if (P.first_layer) {
@@ -604,7 +648,7 @@ MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
       const float* ssq = ph == PH_RP ? P.ssq_mid : P.ssq_out;
       if (tid < P.T) {
         float s = 0.f;
-        for (int j = 0; j < P.H / 128; ++j) s += ssq[j * kMaxT + tid];
+        for (int j = 0; j < P.H / 128; ++j) s += __ldcg(ssq + j * kMaxT + tid);
         m->rnorm[tid] = 1.0f / sqrtf(s / P.H + P.eps);
       }
     } else if (ph == PH_GU) {
@@ -615,13 +659,13 @@ MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
       }
       if (tid < P.T) {
         float a = 0.f;
-        for (int j = 0; j < P.P / 128; ++j) a = fmaxf(a, P.pamax[j * kMaxT + tid]);
+        for (int j = 0; j < P.P / 128; ++j) a = fmaxf(a, __ldcg(P.pamax + j * kMaxT + tid));
         m->srow_st[tid] = a > 0.f ? __fdiv_rn(a, 2688.0f) : 1.0f;
       }
     } else if (ph == PH_DOWN && P.moe) {
       for (int s = tid; s < P.T * P.topk; s += 64) {
         float a = 0.f;
-        for (int j = 0; j < P.I / 128; ++j) a = fmaxf(a, P.aamax[s * (P.I / 128) + j]);
+        for (int j = 0; j < P.I / 128; ++j) a = fmaxf(a, __ldcg(P.aamax + s * (P.I / 128) + j));
         m->srow_st[s] = a > 0.f ? __fdiv_rn(a, 2688.0f) : 1.0f;
       }
     }
@@ -632,18 +676,30 @@ MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
       const uint32_t b = ucount & 1;
       if (!wait_bar(P, S, &m->bempty[b], b_ph[b] ^ 1, ERR_TIMEOUT_B)) { ok = false; break; }
       uint8_t* bb = S.bbuf(b);
+      bool sok = true;
       switch (ph) {
-        case PH_QKV: stage_bf16(P, S, bb, P.x_in, P.H, U.x0, U.nkb, P.attn_norm_w); break;
-        case PH_NQKV: stage_bf16(P, S, bb, P.x_out, P.H, U.x0, U.nkb, P.next_attn_norm_w); break;
-        case PH_O: stage_bf16(P, S, bb, P.o_buf, P.Hq * P.d, U.x0, U.nkb, nullptr); break;
-        case PH_RP: stage_bf16(P, S, bb, P.xmid, P.H, U.x0, U.nkb, P.ffn_norm_w); break;
-        case PH_UNPOOL: stage_bf16(P, S, bb, P.y_buf, P.P, U.x0, U.nkb, nullptr); break;
-        case PH_GU: stage_fp4(P, S, bb, U, true); break;
+        case PH_QKV:
+          sok = stage_bf16(P, S, bb, P.x_in, P.H, U.x0, U.nkb, P.attn_norm_w, land_ph[0]);
+          break;
+        case PH_NQKV:
+          sok = stage_bf16(P, S, bb, P.x_out, P.H, U.x0, U.nkb, P.next_attn_norm_w, land_ph[0]);
+          break;
+        case PH_O:
+          sok = stage_bf16(P, S, bb, P.o_buf, P.Hq * P.d, U.x0, U.nkb, nullptr, land_ph[0]);
+          break;
+        case PH_RP:
+          sok = stage_bf16(P, S, bb, P.xmid, P.H, U.x0, U.nkb, P.ffn_norm_w, land_ph[0]);
+          break;
+        case PH_UNPOOL:
+          sok = stage_bf16(P, S, bb, P.y_buf, P.P, U.x0, U.nkb, nullptr, land_ph[0]);
+          break;
+        case PH_GU: sok = stage_fp4(P, S, bb, U, true, land_ph); break;
         case PH_DOWN:
-          if (P.moe) stage_fp4(P, S, bb, U, false);
-          else stage_bf16(P, S, bb, P.a_buf, P.F, U.x0, U.nkb, nullptr);
+          if (P.moe) sok = stage_fp4(P, S, bb, U, false, land_ph);
+          else sok = stage_bf16(P, S, bb, P.a_buf, P.F, U.x0, U.nkb, nullptr, land_ph[0]);
           break;
       }
+      if (!sok) { ok = false; break; }
       fence_proxy_async_smem();
       stage_sync();
       if (tid == 0) mbar_arrive(&m->bfull[b]);
@@ -690,7 +746,7 @@ MK_DEV void router_topk(const LayerParams& P, int et) {
 #pragma unroll
     for (int i = 0; i < kMaxE / 32; ++i) {
       const int e = lane + 32 * i;
-      v[i] = e < P.E ? lg[e] : -INFINITY;
+      v[i] = e < P.E ? __ldcg(lg + e) : -INFINITY;
       mx = fmaxf(mx, v[i]);
     }
     mx = warp_max(mx);
@@ -774,7 +830,7 @@ MK_DEV void epi_bf16_final(const LayerParams& P, const Smem& S, int ph, const Un
         sq[t] = 0.f;
         if (valid && t < P.T) {
           const size_t o = static_cast<size_t>(t) * P.H + f;
-          const float x = round_bf(bf(res[o]) + g[t]);
+          const float x = round_bf(ld_bf(res + o) + g[t]);
           dst[o] = to_bf(x);
           sq[t] = x * x;
         }
@@ -855,27 +911,29 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
         const int s = m->slots[m->off[e] + i];
         P.z_buf[static_cast<size_t>(s) * P.P + f] = to_bf(g[i] * m->srow_ep[s] * td);
       }
-      __threadfence();
       epi_sync();
       const int tiles = P.P / 128;
       if (et < n) {
         const int s = m->slots[m->off[e] + et];
         const int t = s / P.topk;
         uint32_t* c = P.comb_ctr + t * tiles + U.tile;
+        __threadfence();
         const uint32_t old = atomicAdd(c, 1u);
         const bool last = old == static_cast<uint32_t>(P.topk - 1);
-        if (last) *c = 0;
+        if (last) {
+          *c = 0;
+          __threadfence();
+        }
         m->done[et] = last ? t : -1;
       }
       epi_sync();
       for (int i = 0; i < n; ++i) {
         const int t = m->done[i];
         if (t < 0) continue;
-        __threadfence();
         float acc = 0.f;
         for (int r = 0; r < P.topk; ++r)
-          acc += P.wts[t * P.topk + r] *
-                 bf(P.z_buf[static_cast<size_t>(t * P.topk + r) * P.P + f]);
+          acc += __ldcg(P.wts + t * P.topk + r) *
+                 ld_bf(P.z_buf + static_cast<size_t>(t * P.topk + r) * P.P + f);
         P.y_buf[static_cast<size_t>(t) * P.P + f] = to_bf(acc);
       }
       epi_sync();
@@ -892,24 +950,26 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
       float* dst = P.part + (static_cast<size_t>(U.ks * U.pair + j) * kMaxT) * Npad + col;
       for (int t = 0; t < P.T; ++t) dst[static_cast<size_t>(t) * Npad] = j ? u[t] : g[t];
     }
-    __threadfence();
     epi_sync();
     if (et == 0) {
       uint32_t* c = P.fix_ctr + ph * 256 + U.col_tile;
+      __threadfence();
       const uint32_t old = atomicAdd(c, 1u);
       const bool last = old == static_cast<uint32_t>(U.ksplit - 1);
-      if (last) *c = 0;
+      if (last) {
+        *c = 0;
+        __threadfence();
+      }
       m->flag = last;
     }
     epi_sync();
     if (!m->flag) return true;
-    __threadfence();
     for (int j = 0; j < U.pair; ++j) {
       const float* src = P.part + (static_cast<size_t>(j) * kMaxT) * Npad + col;
       for (int t = 0; t < P.T; ++t) {
         float acc = 0.f;
         for (int ks = 0; ks < U.ksplit; ++ks)
-          acc += src[(static_cast<size_t>(ks * U.pair) * kMaxT + t) * Npad];
+          acc += __ldcg(src + (static_cast<size_t>(ks * U.pair) * kMaxT + t) * Npad);
         (j ? u : g)[t] = acc;
       }
     }
@@ -917,17 +977,19 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
   epi_bf16_final(P, S, ph, U, et, g, u);
   if (ph == PH_RP && P.moe && U.router) {
     // the last finished router tile computes the top-k for every token
-    __threadfence();
     epi_sync();
     if (et == 0) {
+      __threadfence();
       const uint32_t old = atomicAdd(P.misc_ctr, 1u);
       const bool last = old == static_cast<uint32_t>(P.tiles_router - 1);
-      if (last) *P.misc_ctr = 0;
+      if (last) {
+        *P.misc_ctr = 0;
+        __threadfence();
+      }
       m->flag = last;
     }
     epi_sync();
     if (m->flag) {
-      __threadfence();
       router_topk(P, et);
     }
   }
@@ -987,16 +1049,15 @@ MK_DEV void attention_unit(const LayerParams& P, const Smem& S, int g, int lo, i
   const __nv_bfloat16* qsrc = P.first_layer ? P.q_buf : P.q_in;
   const int qld = P.Hq * D;
 
-  // Q tile: row = w*16 + t (q head 4g+w, token t)
+  // Q tile: row = w*16 + t (q head 4g+w, token t); rows t >= T read as zero
   for (int i = et; i < 64 * kChunks; i += 128) {
     const int r = i / kChunks, c = i % kChunks;
     const int hl = r >> 4, t = r & 15;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (t < P.T)
-      v = *reinterpret_cast<const uint4*>(qsrc + static_cast<size_t>(t) * qld +
-                                          (4 * g + hl) * D + c * 8);
-    *reinterpret_cast<uint4*>(sQ + tile_off<D>(r, c)) = v;
+    const bool valid = t < P.T;
+    const __nv_bfloat16* src = qsrc + static_cast<size_t>(valid ? t : 0) * qld + (4 * g + hl) * D + c * 8;
+    cp_async16(smem_u32(sQ + tile_off<D>(r, c)), src, valid);
   }
+  cp_async_commit();
   auto load_kv = [&](int buf, int p0) {
     for (int i = et; i < 64 * kChunks; i += 128) {
       const int r = i / kChunks, c = i % kChunks;
@@ -1009,16 +1070,7 @@ MK_DEV void attention_unit(const LayerParams& P, const Smem& S, int g, int lo, i
     cp_async_commit();
   };
   load_kv(0, lo);
-  epi_sync();
-
-  // Q fragments of this warp (rows w*16 .. w*16+15)
   uint32_t qa[D / 16][4];
-#pragma unroll
-  for (int ks = 0; ks < D / 16; ++ks) {
-    const int r = w * 16 + (lane & 15);
-    const int c = ks * 2 + (lane >> 4);
-    ldsm_x4(smem_u32(sQ + tile_off<D>(r, c)), qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
-  }
   float o[D / 8][4];
 #pragma unroll
   for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
@@ -1038,6 +1090,15 @@ MK_DEV void attention_unit(const LayerParams& P, const Smem& S, int g, int lo, i
       cp_async_wait<0>();
     }
     epi_sync();
+    if (it == 0) {
+      // Q fragments of this warp (rows w*16 .. w*16+15)
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const int r = w * 16 + (lane & 15);
+        const int c = ks * 2 + (lane >> 4);
+        ldsm_x4(smem_u32(sQ + tile_off<D>(r, c)), qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
+      }
+    }
     // S = Q K^T (16 x 64)
     float s[8][4];
 #pragma unroll
@@ -1147,9 +1208,12 @@ MK_DEV void attention_unit(const LayerParams& P, const Smem& S, int g, int lo, i
   }
 }
 
-// Merge of the attention partials of one (token, q head): o = sum_c 2^(m_c-M) o_c / L.
+// Merge of the attention partials of one (token, q head) by one warp:
+// o = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c over the chunks c.
 template <int D>
-MK_DEV void merge_item(const LayerParams& P, int item, int et) {
+MK_DEV void merge_item(const LayerParams& P, int item) {
+  constexpr int V = D / 32;  // output elements per lane
+  const int lane = lane_id();
   const int t = item / P.Hq, hq = item % P.Hq;
   const int g = hq / 4, hl = hq % 4;
   const int row = hl * 16 + t;
@@ -1157,24 +1221,34 @@ MK_DEV void merge_item(const LayerParams& P, int item, int et) {
   const float* base = P.attn_part + static_cast<size_t>(g * P.attn_chunks) * stride +
                       static_cast<size_t>(row) * (D + 2);
   float M = -INFINITY;
-  for (int c = 0; c < P.attn_chunks; ++c) M = fmaxf(M, base[c * stride + D]);
-  if (et >= D) return;
-  float L = 0.f, acc = 0.f;
+  for (int c = lane; c < P.attn_chunks; c += 32) M = fmaxf(M, __ldcg(base + c * stride + D));
+  M = warp_max(M);
+  float acc[V], L = 0.f;
+#pragma unroll
+  for (int v = 0; v < V; ++v) acc[v] = 0.f;
+#pragma unroll 4
   for (int c = 0; c < P.attn_chunks; ++c) {
     const float* pc = base + c * stride;
-    const float mc = pc[D];
-    if (mc == -INFINITY) continue;
-    const float wgt = exp2f(mc - M);
-    L += wgt * pc[D + 1];
-    acc += wgt * pc[et];
+    const float mc = __ldcg(pc + D), lc = __ldcg(pc + D + 1);
+    float ov[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) ov[v] = __ldcg(pc + lane * V + v);
+    const float wgt = mc == -INFINITY ? 0.f : exp2f(mc - M);
+    L += wgt * lc;
+#pragma unroll
+    for (int v = 0; v < V; ++v) acc[v] += wgt * ov[v];
   }
-  P.o_buf[static_cast<size_t>(t) * P.Hq * D + hq * D + et] = to_bf(acc / L);
+  __nv_bfloat16* out = P.o_buf + static_cast<size_t>(t) * P.Hq * D + hq * D + lane * V;
+#pragma unroll
+  for (int v = 0; v < V; ++v) out[v] = to_bf(acc[v] / L);
 }
 
 MK_DEV bool epi_arrive(const LayerParams& P, const Smem& S, int id, int et) {
-  __threadfence();
   epi_sync();
-  if (et == 0) red_release_add(P.bar_ctr + id, 1u);
+  if (et == 0) {
+    __threadfence();
+    red_release_add(P.bar_ctr + id, 1u);
+  }
   return true;
 }
 
@@ -1194,6 +1268,7 @@ MK_DEV void run_epilogue(const LayerParams& P, const Smem& S, uint32_t epoch) {
   for (int ph = 0; ph < PH_COUNT && ok; ++ph) {
     if (!phase_active(P, ph)) continue;
     if (ph == last_ph && et == 0) pdl_launch_dependents();
+    if (et == 0) stamp(P, ph, 0);
     if (ph == PH_ATTN) {
       if (P.first_layer && !(ok = epi_wait(P, S, BAR_QKV, target, et))) break;
       const int n = phase_units(P, S, ph);
@@ -1204,16 +1279,21 @@ MK_DEV void run_epilogue(const LayerParams& P, const Smem& S, uint32_t epoch) {
         if (P.d == 128) attention_unit<128>(P, S, g, lo, hi, c, et);
         else attention_unit<64>(P, S, g, lo, hi, c, et);
       }
+      if (et == 0) stamp(P, ph, 1);
       epi_arrive(P, S, BAR_ATTN, et);
       continue;
     }
     if (ph == PH_MERGE) {
       if (!(ok = epi_wait(P, S, BAR_ATTN, target, et))) break;
       const int n = phase_units(P, S, ph);
-      for (int u = first_unit(P, ph); u < n; u += P.grid) {
-        if (P.d == 128) merge_item<128>(P, u, et);
-        else merge_item<64>(P, u, et);
+      const int w = et >> 5;
+      int k = 0;
+      for (int u = first_unit(P, ph); u < n; u += P.grid, ++k) {
+        if ((k & 3) != w) continue;  // the CTA's k-th item goes to warp k % 4
+        if (P.d == 128) merge_item<128>(P, u);
+        else merge_item<64>(P, u);
       }
+      if (et == 0) stamp(P, ph, 1);
       epi_arrive(P, S, BAR_MERGE, et);
       continue;
     }
@@ -1223,7 +1303,7 @@ MK_DEV void run_epilogue(const LayerParams& P, const Smem& S, uint32_t epoch) {
       if (!(ok = epi_wait(P, S, BAR_RP, target, et))) break;
       if (et < P.T) {
         float a = 0.f;
-        for (int j = 0; j < P.P / 128; ++j) a = fmaxf(a, P.pamax[j * kMaxT + et]);
+        for (int j = 0; j < P.P / 128; ++j) a = fmaxf(a, __ldcg(P.pamax + j * kMaxT + et));
         m->srow_ep[et] = a > 0.f ? __fdiv_rn(a, 2688.0f) : 1.0f;
       }
       epi_sync();
@@ -1231,7 +1311,7 @@ MK_DEV void run_epilogue(const LayerParams& P, const Smem& S, uint32_t epoch) {
       if (!(ok = epi_wait(P, S, BAR_GU, target, et))) break;
       for (int s = et; s < P.T * P.topk; s += 128) {
         float a = 0.f;
-        for (int j = 0; j < P.I / 128; ++j) a = fmaxf(a, P.aamax[s * (P.I / 128) + j]);
+        for (int j = 0; j < P.I / 128; ++j) a = fmaxf(a, __ldcg(P.aamax + s * (P.I / 128) + j));
         m->srow_ep[s] = a > 0.f ? __fdiv_rn(a, 2688.0f) : 1.0f;
       }
       epi_sync();
@@ -1244,6 +1324,7 @@ MK_DEV void run_epilogue(const LayerParams& P, const Smem& S, uint32_t epoch) {
       ++ucount;
     }
     if (!ok) break;
+    if (et == 0) stamp(P, ph, 1);
     epi_arrive(P, S, phase_arrive(P, ph), et);
   }
   // CTA 0 advances the epoch once every CTA has finished this launch.
@@ -1264,6 +1345,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_layer_kernel(const __grid_cons
   S.m = reinterpret_cast<Misc*>(S.base + kOffMisc);
   const int warp = threadIdx.x >> 5;
   Misc* m = S.m;
+  if (threadIdx.x == 0) stamp(P, PH_COUNT, 0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -1278,6 +1360,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_layer_kernel(const __grid_cons
     }
     mbar_init(&m->route_ready, 1);
     mbar_init(&m->mma_done, 1);
+    for (int i = 0; i < 3; ++i) mbar_init(&m->land[i], 1);
     m->abort = 0;
     m->n_act = 0;
     fence_mbar_init();
@@ -1300,6 +1383,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_layer_kernel(const __grid_cons
     // advances the epoch only after every CTA has arrived on the last counter.
     if (threadIdx.x == 32) m->epoch = *reinterpret_cast<volatile uint32_t*>(P.epoch);
     named_bar(3, kThreads - 32);
+    if (threadIdx.x == 32) stamp(P, PH_COUNT, 1);
     const uint32_t epoch = m->epoch;
     if (warp == 1) {
       if (lane_id() == 0) run_mma(P, S);
@@ -1315,6 +1399,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_layer_kernel(const __grid_cons
     tc_fence_after();
     tmem_dealloc(m->tmem_base, kTmemCols);
   }
+  if (threadIdx.x == 0) stamp(P, PH_COUNT, 2);
 }
 
 const void* layer_kernel_ptr() { return reinterpret_cast<const void*>(&mk_layer_kernel); }

@@ -112,6 +112,12 @@ struct LayerParams {
   uint32_t* bar_ctr;        // [kNumCounters] grid dependency counters
   uint32_t* epoch;          // launches of this layer so far
   uint32_t* status;         // sticky error word
+  // self-timing (optional, nullptr when off): %globaltimer stamps per CTA,
+  // [grid][PH_COUNT + 1][4]: per phase (epilogue start, epilogue end, last MMA
+  // issued, last weight tile issued); last row (kernel start, inputs ready,
+  // kernel end, 0)
+  uint64_t* ts;
 };
+constexpr int kTsPerCta = (PH_COUNT + 1) * 4;
 
 }  // namespace mk

@@ -164,7 +164,9 @@ def moe_ffn(h, W, idx, w):
     I = W["exp_gate_q"].shape[1]
     a = np.zeros((T, k, I))
     a_hat = np.zeros((T, k, I))
+    gu = np.zeros((T, k, 2, I))      # gate / up sums before SiLU (float64)
     z = np.zeros((T, k, P))
+    z_acc = np.zeros((T, k, P))      # down sums before rounding (float64)
     for e in sorted(set(int(v) for v in idx.ravel())):
         wg = nvfp4_dequantize(W["exp_gate_q"][e], W["exp_gate_s"][e], W["exp_gate_ts"][e])
         wu = nvfp4_dequantize(W["exp_up_q"][e], W["exp_up_s"][e], W["exp_up_ts"][e])
@@ -175,10 +177,12 @@ def moe_ffn(h, W, idx, w):
                     continue
                 g = wg @ p_hat[t]
                 u = wu @ p_hat[t]
+                gu[t, r, 0], gu[t, r, 1] = g, u
                 a[t, r] = bf16_round(silu(g) * u)
                 aq, as_, arow = nvfp4_quantize_rows(a[t, r][None, :])
                 a_hat[t, r] = nvfp4_dequantize(aq, as_, arow)[0]
-                z[t, r] = bf16_round(wd @ a_hat[t, r])
+                z_acc[t, r] = wd @ a_hat[t, r]
+                z[t, r] = bf16_round(z_acc[t, r])
     wf = np.asarray(w, dtype=np.float32).astype(np.float64)
     y = np.zeros((T, P))
     for t in range(T):
@@ -186,7 +190,7 @@ def moe_ffn(h, W, idx, w):
         for r in range(k):
             acc = acc + wf[t, r] * z[t, r]
         y[t] = bf16_round(acc)
-    return dict(p=p, p_hat=p_hat, a=a, a_hat=a_hat, z=z, y=y)
+    return dict(p=p, p_hat=p_hat, a=a, a_hat=a_hat, gu=gu, z=z, z_acc=z_acc, y=y)
 
 
 def dense_ffn(h, W):
@@ -236,7 +240,8 @@ def layer_forward(cfg, W, x_in, k_cache, v_cache, ctx, q_in=None, first_layer=Tr
         out.update(logits=logits, idx=idx, w=w)
         m = moe_ffn(h, W, idx, w)
         out.update(m)
-        x_out = bf16_round(x_mid + m["y"] @ np.asarray(W["w_unpool"], dtype=np.float64).T)
+        out["x_acc"] = x_mid + m["y"] @ np.asarray(W["w_unpool"], dtype=np.float64).T
+        x_out = bf16_round(out["x_acc"])
     else:
         dres = dense_ffn(h, W)
         out["a"] = dres["a"]

@@ -27,10 +27,29 @@ def metrics(got, ref):
     return dict(rms=rms, maxabs=maxabs, rel=maxabs / rms if rms > 0 else maxabs, cos=cos)
 
 
-def assert_close(name, got, ref):
+def bf16_ulp(x):
+    """Spacing of bfloat16 numbers at |x| (8 significant bits)."""
+    x = np.abs(np.asarray(x, dtype=np.float64))
+    e = np.frexp(np.where(x > 0, x, 1.0))[1]
+    return np.ldexp(1.0, np.maximum(e - 8, -133))
+
+
+def assert_close(name, got, ref, extra_abs=0.0):
+    """max |got - ref| <= 2e-2 * RMS(ref) and cosine >= 0.9995.
+
+    Both sides store bfloat16, so two correct evaluations can differ by one
+    unit in the last place of an element; where that unit exceeds 2e-2 * RMS
+    (elements above ~4 * RMS), the element's own ulp is the bound.
+    `extra_abs` widens the bound by an amount derived from the oracle (see
+    flip_tolerance)."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
     m = metrics(got, ref)
-    assert np.all(np.isfinite(np.asarray(got, dtype=np.float64))), name + ": non-finite"
-    assert m["maxabs"] <= ABS_TOL * m["rms"] and m["cos"] >= COS_TOL, "%s: %s" % (name, m)
+    assert np.all(np.isfinite(got)), name + ": non-finite"
+    bound = np.maximum(ABS_TOL * m["rms"], bf16_ulp(ref)) + extra_abs
+    over = np.abs(got - ref) > bound
+    m["n_over"] = int(over.sum())
+    assert not over.any() and m["cos"] >= COS_TOL, "%s: %s" % (name, m)
     return m
 
 
@@ -107,13 +126,31 @@ def oracle_single_layer(work, T=None, ctx=None, fuse_next=False, Wn=None, renorm
                             next_W=nxt, next_k_cache=nkc, next_v_cache=nvc, renorm=renorm)
 
 
-def compare_single(gpu, ref, T, ctx, fuse_next=False, moe=True):
-    """Asserts the contract; returns the metrics of every compared tensor."""
+def check_router(g_idx, g_w, r_idx, r_w, r_logits):
+    """Router contract: the chosen expert SET of every token bit-exact (the
+    margin between the k-th and (k+1)-th logit makes it unique); the order
+    inside the set is unique only where the chosen logits differ by more than
+    rounding, so the GPU's order must be non-increasing in the oracle's logits
+    up to 1e-3; the weights, matched by expert, within the contract bound."""
+    g_idx = np.asarray(g_idx)
+    assert np.array_equal(np.sort(g_idx, axis=1), np.sort(r_idx, axis=1)), (g_idx, r_idx)
+    lg = np.take_along_axis(np.asarray(r_logits, dtype=np.float64), g_idx.astype(np.int64), axis=1)
+    assert np.all(np.diff(lg, axis=1) <= 1e-3), "router order"
+    pos = np.argsort(g_idx, axis=1)
+    rpos = np.argsort(r_idx, axis=1)
+    gw = np.take_along_axis(np.asarray(g_w), pos, axis=1)
+    rw = np.take_along_axis(np.asarray(r_w), rpos, axis=1)
+    return assert_close("w", gw, rw)
+
+
+def compare_single(gpu, ref, T, ctx, fuse_next=False, moe=True, x_extra=0.0):
+    """Asserts the contract; returns the metrics of every compared tensor.
+    x_extra: per-token widening of the x_out bound (flip_tolerance)."""
     res = {}
     assert gpu["status"] == 0, "device status %d" % gpu["status"]
     if moe:
-        assert np.array_equal(gpu["idx"], ref["idx"]), (gpu["idx"], ref["idx"])
-    res["x_out"] = assert_close("x_out", gpu["x_out"].double().numpy(), ref["x_out"])
+        res["w"] = check_router(gpu["idx"], gpu["w"], ref["idx"], ref["w"], ref["logits"])
+    res["x_out"] = assert_close("x_out", gpu["x_out"].double().numpy(), ref["x_out"], x_extra)
     res["k_rows"] = assert_close("k_rows", gpu["k_cache"][ctx:ctx + T].double().numpy(),
                                  ref["k_cache"][ctx:ctx + T])
     res["v_rows"] = assert_close("v_rows", gpu["v_cache"][ctx:ctx + T].double().numpy(),
