@@ -68,7 +68,7 @@ typedef enum {
 #define MK_TOPK_RENORM   0x4u  /* combine weights renormalised over the top-k    */
 
 typedef struct mk_layer_config {
-  int32_t hidden;         /* H                                                   */
+  int32_t hidden;         /* H, a multiple of 256                                */
   int32_t n_q_heads;      /* Hq; must equal 4 * n_kv_heads                        */
   int32_t n_kv_heads;     /* Hkv                                                 */
   int32_t head_dim;       /* d: 64 or 128                                        */
@@ -202,12 +202,18 @@ mk_status mk_layer_get_info(mk_layer* layer, mk_layer_info* info);
  * "What the 5.9 ms is still spent on": the kernel times itself with
  * %globaltimer stamps written by one lane per block).  Enabled for layers
  * created while the environment holds MK_TIMESTAMPS=1 (else this returns
- * MK_ERR_UNSUPPORTED).  Copies min(n, grid * 40) stamps of the layer's last
- * step to host memory: per CTA, 10 rows of 4 u64 -- rows 0..8 are the phases
+ * MK_ERR_UNSUPPORTED).  Copies min(n, grid * 160) u64 of the layer's last
+ * step to host memory: per CTA, 10 rows of 16 -- rows 0..8 are the phases
  * (QKV, attention, merge, o-proj, router+pool, expert gate/up, expert down,
- * unpool, next QKV) with (epilogue start, epilogue end, last MMA issued, last
- * weight tile issued); row 9 is (kernel start, inputs ready, kernel end, 0).
- * Unused phases read 0.  Synchronous. */
+ * unpool, next QKV) with %globaltimer stamps (epilogue start, epilogue end,
+ * last MMA issued, last weight tile issued) followed by nanoseconds spent
+ * (producer waiting for a free stage, MMA waiting for weights, for the token
+ * operand, for a free accumulator, stager waiting for a free operand buffer,
+ * stager working, epilogue waiting for an accumulator, epilogue working,
+ * MMA issuing);
+ * row 9 starts with (kernel start, inputs ready, kernel end).  Stamps of
+ * unused phases read 0; the nanosecond slots accumulate across steps until
+ * the layer is destroyed.  Synchronous. */
 mk_status mk_get_timestamps(mk_layer* layer, uint64_t* host_buf, size_t n);
 
 #ifdef __cplusplus

@@ -52,7 +52,7 @@ int choose_ksplit(int K) {
 
 mk_status validate_config(const mk_layer_config* c, const mk_layer_weights* w) {
   if (!c || !w) return MK_ERR_INVALID_ARG;
-  if (c->hidden <= 0 || c->hidden % 128) return MK_ERR_UNSUPPORTED;
+  if (c->hidden <= 0 || c->hidden % 256) return MK_ERR_UNSUPPORTED;
   if (c->n_kv_heads <= 0 || c->n_q_heads != 4 * c->n_kv_heads) return MK_ERR_UNSUPPORTED;
   if (c->head_dim != 64 && c->head_dim != 128) return MK_ERR_UNSUPPORTED;
   if (c->window < 0) return MK_ERR_INVALID_ARG;

@@ -64,7 +64,10 @@ struct Misc {
   float srow_st[kMaxT * kMaxK];    // stager: NVFP4 row scales of the phase input
   float srow_ep[kMaxT * kMaxK];    // epilogue: NVFP4 row scales of the phase input
   float red[4][kMaxT];             // epilogue cross-warp reductions
-  int done[kMaxT];                 // epilogue: combine completions
+  uint32_t comb_local[kMaxT][16];  // epilogue: this CTA's z contributions per (token, tile)
+  int done_pairs[kMaxT * 16];      // epilogue: (token, tile) pairs this CTA completes
+  int n_done;
+  int grp_ok[4];                   // shared outcome of a group's wait: [0] stagers, [1] epilogue, [2..3] stager warps
 };
 static_assert(sizeof(Misc) <= 8192, "misc region");
 
@@ -110,8 +113,13 @@ MK_DEV bool wait_bar(const LayerParams& P, const Smem& S, uint64_t* bar, uint32_
 }
 
 MK_DEV void stamp(const LayerParams& P, int ph, int slot) {
-  if (P.ts) P.ts[(static_cast<size_t>(blockIdx.x) * (PH_COUNT + 1) + ph) * 4 + slot] = globaltimer();
+  if (P.ts) P.ts[(static_cast<size_t>(blockIdx.x) * (PH_COUNT + 1) + ph) * kTsSlots + slot] = globaltimer();
 }
+MK_DEV void stamp_add(const LayerParams& P, int ph, int slot, uint64_t ns) {
+  if (P.ts) P.ts[(static_cast<size_t>(blockIdx.x) * (PH_COUNT + 1) + ph) * kTsSlots + slot] += ns;
+}
+// now() only when self-timing is on (0 otherwise)
+MK_DEV uint64_t tnow(const LayerParams& P) { return P.ts ? globaltimer() : 0; }
 
 MK_DEV uint32_t grid_target(const LayerParams& P, uint32_t epoch) {
   return (epoch + 1u) * static_cast<uint32_t>(P.grid);
@@ -134,6 +142,30 @@ MK_DEV bool grid_wait(const LayerParams& P, const Smem& S, int id, uint32_t targ
 }
 
 MK_DEV void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+
+// Waits of a named-barrier group: one leader waits, every member gets the
+// same outcome (a member must never leave the group's barrier sequence while
+// others go on -- that would hang them at the next barrier).
+MK_DEV bool group_mbar_wait(const LayerParams& P, const Smem& S, uint64_t* bar, uint32_t parity,
+                            uint32_t code, bool leader, int bar_id, int n, int slot) {
+  if (leader) S.m->grp_ok[slot] = wait_bar(P, S, bar, parity, code) ? 1 : 0;
+  named_bar(bar_id, n);
+  const bool ok = *reinterpret_cast<volatile int*>(&S.m->grp_ok[slot]) != 0;
+  named_bar(bar_id, n);
+  return ok;
+}
+MK_DEV bool group_grid_wait(const LayerParams& P, const Smem& S, int id, uint32_t target,
+                            bool leader, int bar_id, int n, int slot) {
+  if (leader) {
+    const bool ok = grid_wait(P, S, id, target);
+    if (!ok) atomicExch(&S.m->abort, 1u);
+    S.m->grp_ok[slot] = ok ? 1 : 0;
+  }
+  named_bar(bar_id, n);
+  const bool ok = *reinterpret_cast<volatile int*>(&S.m->grp_ok[slot]) != 0;
+  named_bar(bar_id, n);
+  return ok;
+}
 constexpr int kBarEpi = 1;     // warps 4-7
 constexpr int kBarStage = 2;   // warps 2-3
 MK_DEV void epi_sync() { named_bar(kBarEpi, 128); }
@@ -401,7 +433,9 @@ MK_DEV void run_producer(const LayerParams& P, const Smem& S) {
       const uint32_t bytes = kTileBytes + (U.fp4 ? kSfBytes : 0);
       for (int kb = 0; kb < U.nkb && ok; ++kb) {
         for (int j = 0; j < U.pair; ++j) {
+          const uint64_t w0 = tnow(P);
           if (!wait_bar(P, S, &m->empty[stage], phase ^ 1, ERR_TIMEOUT_EMPTY)) { ok = false; break; }
+          if (P.ts) stamp_add(P, ph, 4, globaltimer() - w0);
           mbar_arrive_expect_tx(&m->full[stage], bytes);
           const int x = U.x0 + kb * (U.fp4 ? 128 : 64);
           tma_load_2d(S.a_tile(stage), U.map[j], &m->full[stage], x, U.row0, pol);
@@ -423,9 +457,18 @@ MK_DEV void run_producer(const LayerParams& P, const Smem& S) {
   }
 }
 
-// ============================================================ MMA (warp 1)
+// ============================================================ MMA (warp 1, lanes 0-3)
+// A 128-byte K-block of a weight tile holds four MMA K-steps (4 x 16 bf16 or
+// 4 x 64 NVFP4 elements).  Lane l of the MMA warp issues K-step l of every
+// K-block (and copies that step's scale factors) into its own accumulator:
+// one warp instruction puts four MMAs in flight, four times what a single
+// issuing thread reaches.  The epilogue adds the four partial accumulators.
+// TMEM columns: accumulators at 128*b + 64*j + 16*l (buffer b, matrix j of a
+// gate/up pair, lane l); scale factors at 256 + 48*r (r = K-block parity):
+// token operand 16 columns, then 16 per weight matrix (4 per lane).
 MK_DEV void run_mma(const LayerParams& P, const Smem& S) {
   Misc* m = S.m;
+  const uint32_t l = lane_id();  // 0..3
   const uint32_t tbase = m->tmem_base;
   uint32_t stage = 0, phase = 0, acc_ph[2] = {0, 0}, b_ph[2] = {0, 0};
   uint32_t ucount = 0, sfreg = 0;
@@ -434,44 +477,49 @@ MK_DEV void run_mma(const LayerParams& P, const Smem& S) {
   for (int ph = 0; ph < PH_COUNT && ok; ++ph) {
     if (!phase_is_gemm(ph) || !phase_active(P, ph)) continue;
     if (P.moe && ph == PH_GU && !route_known) {
-      if (!wait_bar(P, S, &m->route_ready, 0, ERR_TIMEOUT_ROUTE)) { ok = false; break; }
+      if (!__all_sync(0xFu, wait_bar(P, S, &m->route_ready, 0, ERR_TIMEOUT_ROUTE))) { ok = false; break; }
       route_known = true;
     }
     const int n = phase_units(P, S, ph);
     for (int u = first_unit(P, ph); u < n && ok; u += P.grid) {
       const Unit U = make_unit(P, S, ph, u);
       const uint32_t b = ucount & 1;
-      if (!wait_bar(P, S, &m->accempty[b], acc_ph[b] ^ 1, ERR_TIMEOUT_ACC)) { ok = false; break; }
-      if (!wait_bar(P, S, &m->bfull[b], b_ph[b], ERR_TIMEOUT_B)) { ok = false; break; }
+      uint64_t w0 = tnow(P);
+      if (!__all_sync(0xFu, wait_bar(P, S, &m->accempty[b], acc_ph[b] ^ 1, ERR_TIMEOUT_ACC))) { ok = false; break; }
+      uint64_t w1 = tnow(P);
+      if (!__all_sync(0xFu, wait_bar(P, S, &m->bfull[b], b_ph[b], ERR_TIMEOUT_B))) { ok = false; break; }
+      if (P.ts && l == 0) {
+        const uint64_t w2 = globaltimer();
+        stamp_add(P, ph, 7, w1 - w0);
+        stamp_add(P, ph, 6, w2 - w1);
+      }
       tc_fence_after();
-      const uint32_t acc = tbase + 32 * b;
       uint8_t* bb = S.bbuf(b);
       for (int kb = 0; kb < U.nkb && ok; ++kb) {
         for (int j = 0; j < U.pair; ++j) {
-          if (!wait_bar(P, S, &m->full[stage], phase, ERR_TIMEOUT_FULL)) { ok = false; break; }
+          __syncwarp(0xFu);
+          const uint64_t wf = tnow(P);
+          if (!__all_sync(0xFu, wait_bar(P, S, &m->full[stage], phase, ERR_TIMEOUT_FULL))) { ok = false; break; }
+          const uint64_t wi = tnow(P);
+          if (P.ts && l == 0) stamp_add(P, ph, 5, wi - wf);
           tc_fence_after();
-          const uint64_t da = sdesc_kmajor_sw128(smem_u32(S.a_tile(stage)));
-          const uint64_t db = sdesc_kmajor_sw128(smem_u32(bb + kb * 2048));
-          const uint32_t d = acc + 16 * j;
+          __syncwarp(0xFu);
+          const uint64_t da = sdesc_kmajor_sw128(smem_u32(S.a_tile(stage))) + 2 * l;
+          const uint64_t db = sdesc_kmajor_sw128(smem_u32(bb + kb * 2048)) + 2 * l;
+          const uint32_t d = tbase + 128 * b + 64 * j + 16 * l;
           if (U.fp4) {
-            const uint32_t sfa = tbase + 64 + 32 * sfreg, sfb = sfa + 16;
-            sfreg = (sfreg + 1) & 3;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              tmem_cp_sf(sfa + 4 * c, sdesc_sf_chunk(smem_u32(S.sf(stage) + c * 512)));
-              tmem_cp_sf(sfb + 4 * c,
-                         sdesc_sf_chunk(smem_u32(bb + kBSfOff + (kb * 4 + c) * 512)));
-            }
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_nvf4(d, da + 2 * kk, db + 2 * kk, idesc_nvf4(128, kMaxT), sfa + 4 * kk,
-                       sfb + 4 * kk, (kb | kk) != 0);
+            const uint32_t reg = tbase + 256 + 48 * (sfreg & 1);
+            const uint32_t sfb = reg + 4 * l, sfa = reg + 16 + 16 * j + 4 * l;
+            tmem_cp_sf(sfa, sdesc_sf_chunk(smem_u32(S.sf(stage) + l * 512)));
+            if (j == 0)
+              tmem_cp_sf(sfb, sdesc_sf_chunk(smem_u32(bb + kBSfOff + (kb * 4 + l) * 512)));
+            mma_nvf4(d, da, db, idesc_nvf4(128, kMaxT), sfa, sfb, kb != 0);
+            if (j == U.pair - 1) ++sfreg;
           } else {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_bf16(d, da + 2 * kk, db + 2 * kk, idesc_bf16(128, kMaxT), (kb | kk) != 0);
+            mma_bf16(d, da, db, idesc_bf16(128, kMaxT), kb != 0);
           }
           mma_commit(&m->empty[stage]);
+          if (P.ts && l == 0) stamp_add(P, ph, 12, globaltimer() - wi);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
       }
@@ -482,7 +530,7 @@ MK_DEV void run_mma(const LayerParams& P, const Smem& S) {
       b_ph[b] ^= 1;
       ++ucount;
     }
-    stamp(P, ph, 2);
+    if (l == 0) stamp(P, ph, 2);
   }
   // all issued tensor-core work completes before TMEM is released
   mma_commit(&m->mma_done);
@@ -511,7 +559,8 @@ MK_DEV bool stage_bf16(const LayerParams& P, const Smem& S, uint8_t* bb, const _
                 pol);
     if (gain) bulk_load(graw, gain + k0, rowbytes, &S.m->land[0], pol);
   }
-  if (!wait_bar(P, S, &S.m->land[0], land_ph, ERR_TIMEOUT_B)) return false;
+  if (!group_mbar_wait(P, S, &S.m->land[0], land_ph, ERR_TIMEOUT_B, tid == 0, kBarStage, 64, 0))
+    return false;
   land_ph ^= 1;
   const int chunks = nkb * 8;  // 16-byte chunks per row
   for (int i = tid; i < kMaxT * chunks; i += 64) {
@@ -600,13 +649,43 @@ MK_DEV bool stage_fp4(const LayerParams& P, const Smem& S, uint8_t* bb, const Un
       mbar_arrive_expect_tx(lb, rowbytes);
       bulk_load(slot, row, rowbytes, lb, policy_evict_last());
     }
-    if (!wait_bar(P, S, lb, land_ph[1 + warp], ERR_TIMEOUT_B)) return false;
+    int wok = 0;
+    if (lane_id() == 0) wok = wait_bar(P, S, lb, land_ph[1 + warp], ERR_TIMEOUT_B) ? 1 : 0;
+    if (!__shfl_sync(0xffffffffu, wok, 0)) return false;
     land_ph[1 + warp] ^= 1;
     OperandSink sink{bb, bb + kBSfOff, static_cast<uint32_t>(i)};
     quantize_row_given_srow(reinterpret_cast<const __nv_bfloat16*>(slot), K,
                             gu ? m->srow_st[t] : m->srow_st[s], sink);
   }
   return true;
+}
+
+// RMSNorm factors of x_in (first layer), by warps 2..7: one row per warp at a
+// time, each lane's 16-byte loads of the row issued together.
+MK_DEV void rnorm_x_in(const LayerParams& P, const Smem& S) {
+  const int w = (threadIdx.x >> 5) - 2;  // 0..5
+  const int per_lane = P.H / 256;         // 16-byte chunks per lane (H % 256 == 0)
+  for (int t = w; t < P.T; t += 6) {
+    const uint4* x = reinterpret_cast<const uint4*>(P.x_in + static_cast<size_t>(t) * P.H) + lane_id();
+    float s = 0.f;
+    for (int c0 = 0; c0 < per_lane; c0 += 8) {
+      uint4 v[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) v[c] = c0 + c < per_lane ? x[(c0 + c) * 32] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint32_t* pv = reinterpret_cast<const uint32_t*>(&v[c]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float a = __uint_as_float(pv[k] << 16), b = __uint_as_float(pv[k] & 0xFFFF0000u);
+          s += a * a + b * b;
+        }
+      }
+    }
+    s = warp_sum(s);
+    if (lane_id() == 0) S.m->rnorm[t] = 1.0f / sqrtf(s / P.H + P.eps);
+  }
+  named_bar(4, 192);
 }
 
 MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
@@ -616,32 +695,12 @@ MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
   const uint32_t target = grid_target(P, epoch);
   uint32_t b_ph[2] = {0, 0}, ucount = 0, land_ph[3] = {0, 0, 0};
   bool ok = true;
-  // RMSNorm factors of x_in (first layer)
-  if (P.first_layer) {
-    for (int t = warp; t < P.T; t += 2) {
-      const __nv_bfloat16* x = P.x_in + static_cast<size_t>(t) * P.H;
-      float s = 0.f;
-      for (int k = lane_id() * 8; k < P.H; k += 256) {
-        const uint4 v = *reinterpret_cast<const uint4*>(x + k);
-        const uint32_t* pv = reinterpret_cast<const uint32_t*>(&v);
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const float a = __uint_as_float(pv[w] << 16), b2 = __uint_as_float(pv[w] & 0xFFFF0000u);
-          s += a * a + b2 * b2;
-        }
-      }
-      s = warp_sum(s);
-      if (lane_id() == 0) m->rnorm[t] = 1.0f / sqrtf(s / P.H + P.eps);
-    }
-    stage_sync();
-  }
+  if (P.first_layer) rnorm_x_in(P, S);
   for (int ph = 0; ph < PH_COUNT && ok; ++ph) {
     if (!phase_is_gemm(ph) || !phase_active(P, ph)) continue;
     const int dep = phase_dep(P, ph);
     if (dep >= 0) {
-      if (tid == 0 && !grid_wait(P, S, dep, target)) atomicExch(&m->abort, 1u);
-      stage_sync();
-      if (aborted(P, S)) { ok = false; break; }
+      if (!group_grid_wait(P, S, dep, target, tid == 0, kBarStage, 64, 0)) { ok = false; break; }
     }
     // per-phase inputs of the token operand
     if (ph == PH_RP || ph == PH_NQKV) {
@@ -674,7 +733,12 @@ MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
     for (int u = first_unit(P, ph); u < n && ok; u += P.grid) {
       const Unit U = make_unit(P, S, ph, u);
       const uint32_t b = ucount & 1;
-      if (!wait_bar(P, S, &m->bempty[b], b_ph[b] ^ 1, ERR_TIMEOUT_B)) { ok = false; break; }
+      const uint64_t w0 = tnow(P);
+      if (!group_mbar_wait(P, S, &m->bempty[b], b_ph[b] ^ 1, ERR_TIMEOUT_B, tid == 0, kBarStage, 64, 0)) {
+        ok = false;
+        break;
+      }
+      const uint64_t w1 = tnow(P);
       uint8_t* bb = S.bbuf(b);
       bool sok = true;
       switch (ph) {
@@ -699,10 +763,21 @@ MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
           else sok = stage_bf16(P, S, bb, P.a_buf, P.F, U.x0, U.nkb, nullptr, land_ph[0]);
           break;
       }
-      if (!sok) { ok = false; break; }
+      // both stager warps agree on the outcome before the next barrier
+      if (lane_id() == 0) m->grp_ok[2 + warp] = sok ? 1 : 0;
       fence_proxy_async_smem();
       stage_sync();
-      if (tid == 0) mbar_arrive(&m->bfull[b]);
+      if (!(*reinterpret_cast<volatile int*>(&m->grp_ok[2]) && *reinterpret_cast<volatile int*>(&m->grp_ok[3]))) {
+        ok = false;
+        break;
+      }
+      if (tid == 0) {
+        mbar_arrive(&m->bfull[b]);
+        if (P.ts) {
+          stamp_add(P, ph, 8, w1 - w0);
+          stamp_add(P, ph, 9, globaltimer() - w1);
+        }
+      }
       b_ph[b] ^= 1;
       ++ucount;
     }
@@ -713,21 +788,23 @@ MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
 // Cross-warp reduction over the 128 epilogue threads of 16 per-token values:
 // returns, in thread t (< 16), the sum (or max) for token t.
 template <bool kMax>
-MK_DEV float epi_reduce16(const Smem& S, float (&v)[kMaxT], int et) {
+MK_DEV float epi_reduce16(const Smem& S, float (&v)[kMaxT], int et, int n) {
   const int q = et >> 5;
 #pragma unroll
   for (int t = 0; t < kMaxT; ++t) {
-    float x = v[t];
+    if (t < n) {
+      float x = v[t];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float y = __shfl_xor_sync(0xffffffffu, x, o);
-      x = kMax ? fmaxf(x, y) : x + y;
+      for (int o = 16; o > 0; o >>= 1) {
+        const float y = __shfl_xor_sync(0xffffffffu, x, o);
+        x = kMax ? fmaxf(x, y) : x + y;
+      }
+      if (lane_id() == 0) S.m->red[q][t] = x;
     }
-    if (lane_id() == 0) S.m->red[q][t] = x;
   }
   epi_sync();
   float r = 0.f;
-  if (et < kMaxT) {
+  if (et < n) {
     r = S.m->red[0][et];
     for (int w = 1; w < 4; ++w) r = kMax ? fmaxf(r, S.m->red[w][et]) : r + S.m->red[w][et];
   }
@@ -835,7 +912,7 @@ MK_DEV void epi_bf16_final(const LayerParams& P, const Smem& S, int ph, const Un
           sq[t] = x * x;
         }
       }
-      const float r = epi_reduce16<false>(S, sq, et);
+      const float r = epi_reduce16<false>(S, sq, et, P.T);
       if (et < P.T) (ph == PH_O ? P.ssq_mid : P.ssq_out)[U.tile * kMaxT + et] = r;
       break;
     }
@@ -860,7 +937,7 @@ MK_DEV void epi_bf16_final(const LayerParams& P, const Smem& S, int ph, const Un
             am[t] = fabsf(x);
           }
         }
-        const float r = epi_reduce16<true>(S, am, et);
+        const float r = epi_reduce16<true>(S, am, et, P.T);
         if (et < P.T) P.pamax[U.tile * kMaxT + et] = r;
       }
       break;
@@ -872,14 +949,28 @@ MK_DEV void epi_bf16_final(const LayerParams& P, const Smem& S, int ph, const Un
 MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Unit& U,
                           uint32_t b, uint32_t& acc_ph_b, int et) {
   Misc* m = S.m;
-  if (!wait_bar(P, S, &m->accfull[b], acc_ph_b, ERR_TIMEOUT_ACC)) return false;
+  const uint64_t w0 = tnow(P);
+  if (!group_mbar_wait(P, S, &m->accfull[b], acc_ph_b, ERR_TIMEOUT_ACC, et == 0, kBarEpi, 128, 1))
+    return false;
+  if (P.ts && et == 0) stamp_add(P, ph, 10, globaltimer() - w0);
   acc_ph_b ^= 1;
   tc_fence_after();
   const int q = et >> 5;
-  const uint32_t taddr = m->tmem_base + (static_cast<uint32_t>(32 * q) << 16) + 32 * b;
+  const uint32_t taddr = m->tmem_base + (static_cast<uint32_t>(32 * q) << 16) + 128 * b;
   float g[kMaxT], u[kMaxT];
-  tmem_ld16(taddr, g);
-  if (U.pair == 2) tmem_ld16(taddr + 16, u);
+  // the four MMA lanes' partial sums (K-steps 0..3 of every K-block)
+  auto load_sum = [&](uint32_t col, float (&acc)[kMaxT]) {
+    tmem_ld16(col, acc);
+#pragma unroll 1
+    for (int l = 1; l < 4; ++l) {
+      float v[kMaxT];
+      tmem_ld16(col + 16 * l, v);
+#pragma unroll
+      for (int t = 0; t < kMaxT; ++t) acc[t] += v[t];
+    }
+  };
+  load_sum(taddr, g);
+  if (U.pair == 2) load_sum(taddr + 64, u);
   tc_fence_before();
   __syncwarp();
   if (lane_id() == 0) mbar_arrive(&m->accempty[b]);
@@ -903,7 +994,7 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
           am[i] = fabsf(a);
         }
       }
-      const float r = epi_reduce16<true>(S, am, et);
+      const float r = epi_reduce16<true>(S, am, et, n);
       if (et < n) P.aamax[m->slots[m->off[e] + et] * (P.I / 128) + U.tile] = r;
     } else {
       const float td = P.ts_down[e];
@@ -911,44 +1002,22 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
         const int s = m->slots[m->off[e] + i];
         P.z_buf[static_cast<size_t>(s) * P.P + f] = to_bf(g[i] * m->srow_ep[s] * td);
       }
-      epi_sync();
-      const int tiles = P.P / 128;
-      if (et < n) {
-        const int s = m->slots[m->off[e] + et];
-        const int t = s / P.topk;
-        uint32_t* c = P.comb_ctr + t * tiles + U.tile;
-        __threadfence();
-        const uint32_t old = atomicAdd(c, 1u);
-        const bool last = old == static_cast<uint32_t>(P.topk - 1);
-        if (last) {
-          *c = 0;
-          __threadfence();
-        }
-        m->done[et] = last ? t : -1;
-      }
-      epi_sync();
-      for (int i = 0; i < n; ++i) {
-        const int t = m->done[i];
-        if (t < 0) continue;
-        float acc = 0.f;
-        for (int r = 0; r < P.topk; ++r)
-          acc += __ldcg(P.wts + t * P.topk + r) *
-                 ld_bf(P.z_buf + static_cast<size_t>(t * P.topk + r) * P.P + f);
-        P.y_buf[static_cast<size_t>(t) * P.P + f] = to_bf(acc);
-      }
-      epi_sync();
+      if (et < n) atomicAdd(&m->comb_local[m->slots[m->off[e] + et] / P.topk][U.tile], 1u);
     }
     return true;
   }
 
   // bf16 phase: split-K partials + fix-up by the last arriving unit of a tile
   if (U.ksplit > 1) {
-    // partials: part[ks][j][t][col], col = col_tile * 128 + row in tile
-    const size_t Npad = static_cast<size_t>(U.col_tiles) * 128;
+    // partials: part[ks][j][col][16 tokens], col = col_tile * 128 + row in
+    // tile: each thread moves its 16 token values as four 16-byte vectors
+    const size_t ncol = static_cast<size_t>(U.col_tiles) * 128;
     const int col = U.col_tile * 128 + et;
     for (int j = 0; j < U.pair; ++j) {
-      float* dst = P.part + (static_cast<size_t>(U.ks * U.pair + j) * kMaxT) * Npad + col;
-      for (int t = 0; t < P.T; ++t) dst[static_cast<size_t>(t) * Npad] = j ? u[t] : g[t];
+      float4* dst = reinterpret_cast<float4*>(P.part + ((static_cast<size_t>(U.ks * U.pair + j)) * ncol + col) * kMaxT);
+      const float* v = j ? u : g;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
     }
     epi_sync();
     if (et == 0) {
@@ -965,13 +1034,35 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
     epi_sync();
     if (!m->flag) return true;
     for (int j = 0; j < U.pair; ++j) {
-      const float* src = P.part + (static_cast<size_t>(j) * kMaxT) * Npad + col;
-      for (int t = 0; t < P.T; ++t) {
-        float acc = 0.f;
-        for (int ks = 0; ks < U.ksplit; ++ks)
-          acc += __ldcg(src + (static_cast<size_t>(ks * U.pair) * kMaxT + t) * Npad);
-        (j ? u : g)[t] = acc;
+      float acc[kMaxT];
+#pragma unroll
+      for (int t = 0; t < kMaxT; ++t) acc[t] = 0.f;
+      for (int ks = 0; ks < U.ksplit; ks += 4) {
+        float4 v[4][4];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          if (ks + kk < U.ksplit) {
+            const float4* src = reinterpret_cast<const float4*>(
+                P.part + ((static_cast<size_t>((ks + kk) * U.pair + j)) * ncol + col) * kMaxT);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) v[kk][q] = __ldcg(src + q);
+          }
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          if (ks + kk < U.ksplit) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              acc[4 * q] += v[kk][q].x;
+              acc[4 * q + 1] += v[kk][q].y;
+              acc[4 * q + 2] += v[kk][q].z;
+              acc[4 * q + 3] += v[kk][q].w;
+            }
+          }
+        }
       }
+#pragma unroll
+      for (int t = 0; t < kMaxT; ++t) (j ? u : g)[t] = acc[t];
     }
   }
   epi_bf16_final(P, S, ph, U, et, g, u);
@@ -1243,6 +1334,51 @@ MK_DEV void merge_item(const LayerParams& P, int item) {
   for (int v = 0; v < V; ++v) out[v] = to_bf(acc[v] / L);
 }
 
+// End of the expert-down phase: publish this CTA's z contributions per
+// (token, output tile) with one release, and combine every (token, tile) whose
+// k contributions are now all written: y = bf16(sum_r w[t][r] z[t*k + r]),
+// summed in rank order (page "Muse Spark Open ...", section "What the 5.9 ms
+// is still spent on": the combine).
+MK_DEV void combine_phase_end(const LayerParams& P, const Smem& S, int et) {
+  Misc* m = S.m;
+  const int tiles = P.P / 128;
+  if (et == 0) m->n_done = 0;
+  epi_sync();
+  if (et == 0) __threadfence();
+  epi_sync();
+  for (int i = et; i < P.T * tiles; i += 128) {
+    const int t = i / tiles, j = i % tiles;
+    const uint32_t c = m->comb_local[t][j];
+    if (c == 0) continue;
+    uint32_t* ctr = P.comb_ctr + t * tiles + j;
+    const uint32_t old = atomicAdd(ctr, c);
+    if (old + c == static_cast<uint32_t>(P.topk)) {
+      *ctr = 0;
+      __threadfence();
+      m->done_pairs[atomicAdd(&m->n_done, 1)] = i;
+    }
+  }
+  epi_sync();
+  const int nd = m->n_done;
+  for (int d = 0; d < nd; ++d) {
+    const int i = m->done_pairs[d];
+    const int t = i / tiles, f = (i % tiles) * 128 + et;
+    float z[kMaxK], wr[kMaxK];
+#pragma unroll
+    for (int r = 0; r < kMaxK; ++r) {
+      if (r < P.topk) {
+        z[r] = ld_bf(P.z_buf + static_cast<size_t>(t * P.topk + r) * P.P + f);
+        wr[r] = __ldcg(P.wts + t * P.topk + r);
+      }
+    }
+    float acc = 0.f;
+#pragma unroll
+    for (int r = 0; r < kMaxK; ++r)
+      if (r < P.topk) acc += wr[r] * z[r];
+    P.y_buf[static_cast<size_t>(t) * P.P + f] = to_bf(acc);
+  }
+}
+
 MK_DEV bool epi_arrive(const LayerParams& P, const Smem& S, int id, int et) {
   epi_sync();
   if (et == 0) {
@@ -1253,9 +1389,7 @@ MK_DEV bool epi_arrive(const LayerParams& P, const Smem& S, int id, int et) {
 }
 
 MK_DEV bool epi_wait(const LayerParams& P, const Smem& S, int id, uint32_t target, int et) {
-  if (et == 0 && !grid_wait(P, S, id, target)) atomicExch(&S.m->abort, 1u);
-  epi_sync();
-  return !aborted(P, S);
+  return group_grid_wait(P, S, id, target, et == 0, kBarEpi, 128, 1);
 }
 
 MK_DEV void run_epilogue(const LayerParams& P, const Smem& S, uint32_t epoch) {
@@ -1264,6 +1398,7 @@ MK_DEV void run_epilogue(const LayerParams& P, const Smem& S, uint32_t epoch) {
   const uint32_t target = grid_target(P, epoch);
   uint32_t acc_ph[2] = {0, 0}, ucount = 0;
   bool ok = true;
+  if (P.first_layer) rnorm_x_in(P, S);
   const int last_ph = P.fuse_next ? PH_NQKV : (P.moe ? PH_UNPOOL : PH_DOWN);
   for (int ph = 0; ph < PH_COUNT && ok; ++ph) {
     if (!phase_active(P, ph)) continue;
@@ -1299,7 +1434,8 @@ MK_DEV void run_epilogue(const LayerParams& P, const Smem& S, uint32_t epoch) {
     }
     // GEMM phases: inputs the epilogue itself reads
     if (ph == PH_GU) {
-      if (!(ok = wait_bar(P, S, &m->route_ready, 0, ERR_TIMEOUT_ROUTE))) break;
+      if (!(ok = group_mbar_wait(P, S, &m->route_ready, 0, ERR_TIMEOUT_ROUTE, et == 0, kBarEpi, 128, 1)))
+        break;
       if (!(ok = epi_wait(P, S, BAR_RP, target, et))) break;
       if (et < P.T) {
         float a = 0.f;
@@ -1309,6 +1445,7 @@ MK_DEV void run_epilogue(const LayerParams& P, const Smem& S, uint32_t epoch) {
       epi_sync();
     } else if (ph == PH_DOWN && P.moe) {
       if (!(ok = epi_wait(P, S, BAR_GU, target, et))) break;
+      for (int i = et; i < kMaxT * 16; i += 128) (&m->comb_local[0][0])[i] = 0;
       for (int s = et; s < P.T * P.topk; s += 128) {
         float a = 0.f;
         for (int j = 0; j < P.I / 128; ++j) a = fmaxf(a, __ldcg(P.aamax + s * (P.I / 128) + j));
@@ -1320,10 +1457,13 @@ MK_DEV void run_epilogue(const LayerParams& P, const Smem& S, uint32_t epoch) {
     for (int u = first_unit(P, ph); u < n && ok; u += P.grid) {
       const Unit U = make_unit(P, S, ph, u);
       const uint32_t b = ucount & 1;
+      const uint64_t w0 = tnow(P);
       ok = epi_gemm_unit(P, S, ph, U, b, acc_ph[b], et);
+      if (P.ts && et == 0) stamp_add(P, ph, 11, globaltimer() - w0);
       ++ucount;
     }
     if (!ok) break;
+    if (ph == PH_DOWN && P.moe) combine_phase_end(P, S, et);
     if (et == 0) stamp(P, ph, 1);
     epi_arrive(P, S, phase_arrive(P, ph), et);
   }
@@ -1348,18 +1488,19 @@ __global__ void __launch_bounds__(kThreads, 1) mk_layer_kernel(const __grid_cons
   if (threadIdx.x == 0) stamp(P, PH_COUNT, 0);
 
   if (threadIdx.x == 0) {
+    // barriers completed by tcgen05.commit count the four MMA lanes
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&m->full[s], 1);
-      mbar_init(&m->empty[s], 1);
+      mbar_init(&m->empty[s], 4);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&m->bfull[b], 1);
-      mbar_init(&m->bempty[b], 1);
-      mbar_init(&m->accfull[b], 1);
+      mbar_init(&m->bempty[b], 4);
+      mbar_init(&m->accfull[b], 4);
       mbar_init(&m->accempty[b], 4);
     }
     mbar_init(&m->route_ready, 1);
-    mbar_init(&m->mma_done, 1);
+    mbar_init(&m->mma_done, 4);
     for (int i = 0; i < 3; ++i) mbar_init(&m->land[i], 1);
     m->abort = 0;
     m->n_act = 0;
@@ -1386,7 +1527,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_layer_kernel(const __grid_cons
     if (threadIdx.x == 32) stamp(P, PH_COUNT, 1);
     const uint32_t epoch = m->epoch;
     if (warp == 1) {
-      if (lane_id() == 0) run_mma(P, S);
+      if (lane_id() < 4) run_mma(P, S);
     } else if (warp < 4) {
       run_stager(P, S, epoch);
     } else {

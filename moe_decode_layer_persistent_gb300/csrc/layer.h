@@ -13,7 +13,7 @@ constexpr int kKC = 512;          // K elements per split-K unit (bf16 phases)
 constexpr int kMaxT = 16;         // verify tokens per step (MMA N)
 constexpr int kMaxE = 256;
 constexpr int kMaxK = 8;          // top-k
-constexpr int kTmemCols = 256;
+constexpr int kTmemCols = 512;
 constexpr int kNumCounters = 16;  // grid-wide dependency counters
 
 // Phases of one launch, in order.
@@ -113,11 +113,16 @@ struct LayerParams {
   uint32_t* epoch;          // launches of this layer so far
   uint32_t* status;         // sticky error word
   // self-timing (optional, nullptr when off): %globaltimer stamps per CTA,
-  // [grid][PH_COUNT + 1][4]: per phase (epilogue start, epilogue end, last MMA
-  // issued, last weight tile issued); last row (kernel start, inputs ready,
-  // kernel end, 0)
+  // [grid][PH_COUNT + 1][kTsSlots]: per phase 0 epilogue start, 1 epilogue
+  // end, 2 last MMA issued, 3 last weight tile issued, then nanoseconds spent
+  // 4 producer waiting for a free stage, 5 MMA waiting for weights, 6 MMA
+  // waiting for the token operand, 7 MMA waiting for a free accumulator,
+  // 8 stager waiting for a free operand buffer, 9 stager working, 10 epilogue
+  // waiting for an accumulator, 11 epilogue working; last row: kernel start,
+  // inputs ready, kernel end; 12 MMA issuing (weights ready to commit).
   uint64_t* ts;
 };
-constexpr int kTsPerCta = (PH_COUNT + 1) * 4;
+constexpr int kTsSlots = 16;
+constexpr int kTsPerCta = (PH_COUNT + 1) * kTsSlots;
 
 }  // namespace mk

@@ -202,6 +202,25 @@ MK_DEV void tmem_cp_sf(uint32_t taddr, uint64_t sdesc) {
                : "memory");
 }
 
+// Copy 128 rows x 16 bytes (rows = TMEM lanes, 4 columns each).
+MK_DEV void tmem_cp_128x128b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x128b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+// Copy 128 rows x 32 bytes (rows = TMEM lanes, 8 columns each).
+MK_DEV void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+// Descriptor of a no-swizzle K-major operand: 8-row x 16-byte core matrices,
+// `lbo` bytes apart along K and `sbo` bytes apart along the rows.
+MK_DEV uint64_t sdesc_interleave(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo & 0x3FFFFu) >> 4) << 16;
+  d |= static_cast<uint64_t>((sbo & 0x3FFFFu) >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+
 // 32 lanes x 16 columns of 32-bit: this thread's TMEM lane, columns c..c+15.
 MK_DEV void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];

@@ -207,7 +207,8 @@ def flip_tolerance_fast(cfg, W, ref):
     """Same bound as flip_tolerance, computed by propagating each single
     decision change through the token's expert path with the float64 sums the
     oracle kept (gate/up sums, down sums, unpooler sums): exact for the one
-    changed decision, cheap at the full expert shapes."""
+    changed decision; the candidates of a token are propagated together as
+    matrix products."""
     from oracle import numerics as n
     from oracle.layer import silu
     idx, w = ref["idx"], np.asarray(ref["w"], dtype=np.float64)
@@ -222,43 +223,44 @@ def flip_tolerance_fast(cfg, W, ref):
 
     wun = np.asarray(W["w_unpool"], dtype=np.float64)
     out = np.zeros(T)
-
-    def x_change(t, z_new):
-        y2 = n.bf16_round(sum(w[t, r] * z_new[r] for r in range(k)))
-        dy = y2 - ref["y"][t]
-        nz = np.nonzero(dy)[0]
-        if nz.size == 0:
-            return 0.0
-        x2 = n.bf16_round(ref["x_acc"][t] + wun[:, nz] @ dy[nz])
-        return float(np.max(np.abs(x2 - ref["x_out"][t])))
-
-    def z_from_a(t, r, a_new):
-        if np.array_equal(a_new, ref["a"][t, r]):
-            return ref["z"][t, r]
-        ah = _quantize_dequantize_row(a_new)
-        da = ah - ref["a_hat"][t, r]
-        nz = np.nonzero(da)[0]
-        wd = mats(int(idx[t, r]))[2]
-        return n.bf16_round(ref["z_acc"][t, r] + wd[:, nz] @ da[nz])
-
     for t in range(T):
-        z_base = [ref["z"][t, r] for r in range(k)]
+        zb = np.stack([ref["z"][t, r] for r in range(k)])          # [k, P]
+        Z = []                                                      # candidate z rows [k, P]
+        # pooled-row decisions: every expert of the token sees the change
         _, alts = _row_decisions(ref["p"][t])
         for ii, vals in alts:
             dp = vals - ref["p_hat"][t][ii]
-            zr = []
+            zr = zb.copy()
             for r in range(k):
-                wg, wu, _ = mats(int(idx[t, r]))
+                wg, wu, wd = mats(int(idx[t, r]))
                 g = ref["gu"][t, r, 0] + wg[:, ii] @ dp
                 u = ref["gu"][t, r, 1] + wu[:, ii] @ dp
-                zr.append(z_from_a(t, r, n.bf16_round(silu(g) * u)))
-            out[t] = max(out[t], x_change(t, zr))
+                a2 = n.bf16_round(silu(g) * u)
+                if np.array_equal(a2, ref["a"][t, r]):
+                    continue
+                da = _quantize_dequantize_row(a2) - ref["a_hat"][t, r]
+                nz = np.nonzero(da)[0]
+                zr[r] = n.bf16_round(ref["z_acc"][t, r] + wd[:, nz] @ da[nz])
+            Z.append(zr)
+        # SwiGLU-row decisions: one expert's z changes
         for r in range(k):
             _, alts = _row_decisions(ref["a"][t, r])
+            if not alts:
+                continue
             wd = mats(int(idx[t, r]))[2]
-            for ii, vals in alts:
-                da = vals - ref["a_hat"][t, r][ii]
-                zr = list(z_base)
-                zr[r] = n.bf16_round(ref["z_acc"][t, r] + wd[:, ii] @ da)
-                out[t] = max(out[t], x_change(t, zr))
+            DA = np.zeros((len(alts), ref["a_hat"].shape[2]))
+            for ci, (ii, vals) in enumerate(alts):
+                DA[ci, ii] = vals - ref["a_hat"][t, r][ii]
+            zr_all = n.bf16_round(ref["z_acc"][t, r][None, :] + DA @ wd.T)
+            for ci in range(len(alts)):
+                zr = zb.copy()
+                zr[r] = zr_all[ci]
+                Z.append(zr)
+        if not Z:
+            continue
+        Z = np.stack(Z)                                             # [c, k, P]
+        Y = n.bf16_round(np.einsum("r,crp->cp", w[t], Z))
+        DY = Y - ref["y"][t][None, :]
+        X = n.bf16_round(ref["x_acc"][t][None, :] + DY @ wun.T)
+        out[t] = float(np.max(np.abs(X - ref["x_out"][t][None, :])))
     return out
