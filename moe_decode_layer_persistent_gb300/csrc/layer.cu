@@ -8,17 +8,19 @@
 // (loading, tensor cores, math).  Section "Three bills a kernel this big has to
 // pay": weights are streamed ahead of use into a shared-memory ring.
 //
-// Roles (one CTA of 256 threads per SM):
+// Roles (one CTA of 384 threads per SM):
 //   warp 0      TMA producer: streams 128-row weight tiles (and NVFP4 scale
 //               factors) of every phase into a kStages-deep ring; it never
 //               waits on activations, only on the router for expert tiles.
-//   warp 1      tcgen05 MMA issuer (one thread): weights are operand A (M=128
-//               rows), the T verify tokens operand B (N=16), fp32 accumulators
-//               in tensor memory, two accumulator buffers.
-//   warps 2-3   stagers: wait for a phase's inputs, then write the token
+//   warps 1-4   tcgen05 MMA issuers (one thread each, K-step w-1 of every
+//               K-block): weights are operand A (M=128 rows), the T verify
+//               tokens operand B (N=16), fp32 accumulators in tensor memory,
+//               two accumulator buffers.
+//   warps 5-6   stagers: wait for a phase's inputs, then write the token
 //               operand (RMSNorm applied, or NVFP4-quantised) into shared
 //               memory in the MMA's swizzled layout.
-//   warps 4-7   epilogue (TMEM lanes 0-127) and math: split-K fix-ups,
+//   warp 7      spare (takes part in CTA-wide synchronisation only).
+//   warps 8-11  epilogue (TMEM lanes 0-127) and math: split-K fix-ups,
 //               residuals, router top-k, SwiGLU, combine; attention with
 //               warp-level MMA in the attention phase.
 // Phases are separated by grid-wide dependency counters with bounded waits.
@@ -27,6 +29,10 @@
 #include "quant.cuh"
 
 namespace mk {
+
+// ------------------------------------------------------------ roles
+constexpr int kStagerBase = 160;   // warps 5-6
+constexpr int kEpiBase = 256;      // warps 8-11 (TMEM lane quadrants 0-3)
 
 // ------------------------------------------------------------ smem layout
 constexpr uint32_t kTileBytes = 16384;                       // 128 rows x 128 B
@@ -457,18 +463,19 @@ MK_DEV void run_producer(const LayerParams& P, const Smem& S) {
   }
 }
 
-// ============================================================ MMA (warp 1, lanes 0-3)
+// ============================================================ MMA (warps 1-4, one thread each)
 // A 128-byte K-block of a weight tile holds four MMA K-steps (4 x 16 bf16 or
-// 4 x 64 NVFP4 elements).  Lane l of the MMA warp issues K-step l of every
-// K-block (and copies that step's scale factors) into its own accumulator:
-// one warp instruction puts four MMAs in flight, four times what a single
-// issuing thread reaches.  The epilogue adds the four partial accumulators.
+// 4 x 64 NVFP4 elements).  MMA warp l+1 issues K-step l of every K-block (and
+// copies that step's scale factors) into its own accumulator: a thread waits
+// ~100-200 cycles per tcgen05 instruction it issues, and four issuing warps
+// keep four times as many in flight.  The epilogue adds the four partial
+// accumulators.
 // TMEM columns: accumulators at 128*b + 64*j + 16*l (buffer b, matrix j of a
 // gate/up pair, lane l); scale factors at 256 + 48*r (r = K-block parity):
 // token operand 16 columns, then 16 per weight matrix (4 per lane).
 MK_DEV void run_mma(const LayerParams& P, const Smem& S) {
   Misc* m = S.m;
-  const uint32_t l = lane_id();  // 0..3
+  const uint32_t l = (threadIdx.x >> 5) - 1;  // 0..3
   const uint32_t tbase = m->tmem_base;
   uint32_t stage = 0, phase = 0, acc_ph[2] = {0, 0}, b_ph[2] = {0, 0};
   uint32_t ucount = 0, sfreg = 0;
@@ -477,7 +484,7 @@ MK_DEV void run_mma(const LayerParams& P, const Smem& S) {
   for (int ph = 0; ph < PH_COUNT && ok; ++ph) {
     if (!phase_is_gemm(ph) || !phase_active(P, ph)) continue;
     if (P.moe && ph == PH_GU && !route_known) {
-      if (!__all_sync(0xFu, wait_bar(P, S, &m->route_ready, 0, ERR_TIMEOUT_ROUTE))) { ok = false; break; }
+      if (!wait_bar(P, S, &m->route_ready, 0, ERR_TIMEOUT_ROUTE)) { ok = false; break; }
       route_known = true;
     }
     const int n = phase_units(P, S, ph);
@@ -485,9 +492,9 @@ MK_DEV void run_mma(const LayerParams& P, const Smem& S) {
       const Unit U = make_unit(P, S, ph, u);
       const uint32_t b = ucount & 1;
       uint64_t w0 = tnow(P);
-      if (!__all_sync(0xFu, wait_bar(P, S, &m->accempty[b], acc_ph[b] ^ 1, ERR_TIMEOUT_ACC))) { ok = false; break; }
+      if (!wait_bar(P, S, &m->accempty[b], acc_ph[b] ^ 1, ERR_TIMEOUT_ACC)) { ok = false; break; }
       uint64_t w1 = tnow(P);
-      if (!__all_sync(0xFu, wait_bar(P, S, &m->bfull[b], b_ph[b], ERR_TIMEOUT_B))) { ok = false; break; }
+      if (!wait_bar(P, S, &m->bfull[b], b_ph[b], ERR_TIMEOUT_B)) { ok = false; break; }
       if (P.ts && l == 0) {
         const uint64_t w2 = globaltimer();
         stamp_add(P, ph, 7, w1 - w0);
@@ -497,13 +504,11 @@ MK_DEV void run_mma(const LayerParams& P, const Smem& S) {
       uint8_t* bb = S.bbuf(b);
       for (int kb = 0; kb < U.nkb && ok; ++kb) {
         for (int j = 0; j < U.pair; ++j) {
-          __syncwarp(0xFu);
           const uint64_t wf = tnow(P);
-          if (!__all_sync(0xFu, wait_bar(P, S, &m->full[stage], phase, ERR_TIMEOUT_FULL))) { ok = false; break; }
+          if (!wait_bar(P, S, &m->full[stage], phase, ERR_TIMEOUT_FULL)) { ok = false; break; }
           const uint64_t wi = tnow(P);
           if (P.ts && l == 0) stamp_add(P, ph, 5, wi - wf);
           tc_fence_after();
-          __syncwarp(0xFu);
           const uint64_t da = sdesc_kmajor_sw128(smem_u32(S.a_tile(stage))) + 2 * l;
           const uint64_t db = sdesc_kmajor_sw128(smem_u32(bb + kb * 2048)) + 2 * l;
           const uint32_t d = tbase + 128 * b + 64 * j + 16 * l;
@@ -547,7 +552,7 @@ MK_DEV void run_mma(const LayerParams& P, const Smem& S) {
 // bf16(x * rnorm[t] * gain[k]) when a gain is given.  Rows >= T are zero.
 MK_DEV bool stage_bf16(const LayerParams& P, const Smem& S, uint8_t* bb, const __nv_bfloat16* src,
                        int ld, int k0, int nkb, const __nv_bfloat16* gain, uint32_t& land_ph) {
-  const int tid = threadIdx.x - 64;
+  const int tid = threadIdx.x - kStagerBase;
   uint8_t* raw = bb + kLandOff;
   uint8_t* graw = raw + kMaxT * nkb * 128;
   const uint32_t rowbytes = static_cast<uint32_t>(nkb) * 128u;
@@ -620,13 +625,13 @@ MK_DEV void quantize_row_given_srow(const __nv_bfloat16* row, int K, float s_row
 MK_DEV bool stage_fp4(const LayerParams& P, const Smem& S, uint8_t* bb, const Unit& U, bool gu,
                       uint32_t (&land_ph)[3]) {
   Misc* m = S.m;
-  const int warp = (threadIdx.x >> 5) - 2;  // 0..1
+  const int warp = (threadIdx.x - kStagerBase) >> 5;  // 0..1
   const int e = U.expert;
   const int n = m->off[e + 1] - m->off[e];
   const int K = U.K;
   // K-block padding beyond K must read as zero codes and zero scales
   if (K % 256) {
-    const int tid = threadIdx.x - 64;
+    const int tid = threadIdx.x - kStagerBase;
     const int kb = K / 256, pad_from = (K % 256) / 2;  // bytes of the last K-block row in use
     for (int i = tid; i < kMaxT * 128; i += 64) {
       const int r = i / 128, byte = i % 128;
@@ -660,10 +665,11 @@ MK_DEV bool stage_fp4(const LayerParams& P, const Smem& S, uint8_t* bb, const Un
   return true;
 }
 
-// RMSNorm factors of x_in (first layer), by warps 2..7: one row per warp at a
+// RMSNorm factors of x_in (first layer), by the stager and epilogue warps: one row per warp at a
 // time, each lane's 16-byte loads of the row issued together.
 MK_DEV void rnorm_x_in(const LayerParams& P, const Smem& S) {
-  const int w = (threadIdx.x >> 5) - 2;  // 0..5
+  const int wid = threadIdx.x >> 5;
+  const int w = wid >= kEpiBase / 32 ? wid - kEpiBase / 32 + 2 : wid - kStagerBase / 32;  // 0..5
   const int per_lane = P.H / 256;         // 16-byte chunks per lane (H % 256 == 0)
   for (int t = w; t < P.T; t += 6) {
     const uint4* x = reinterpret_cast<const uint4*>(P.x_in + static_cast<size_t>(t) * P.H) + lane_id();
@@ -690,7 +696,7 @@ MK_DEV void rnorm_x_in(const LayerParams& P, const Smem& S) {
 
 MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
   Misc* m = S.m;
-  const int tid = threadIdx.x - 64;  // 0..63
+  const int tid = threadIdx.x - kStagerBase;  // 0..63
   const int warp = tid >> 5;
   const uint32_t target = grid_target(P, epoch);
   uint32_t b_ph[2] = {0, 0}, ucount = 0, land_ph[3] = {0, 0, 0};
@@ -1161,7 +1167,6 @@ MK_DEV void attention_unit(const LayerParams& P, const Smem& S, int g, int lo, i
     cp_async_commit();
   };
   load_kv(0, lo);
-  uint32_t qa[D / 16][4];
   float o[D / 8][4];
 #pragma unroll
   for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
@@ -1181,97 +1186,99 @@ MK_DEV void attention_unit(const LayerParams& P, const Smem& S, int g, int lo, i
       cp_async_wait<0>();
     }
     epi_sync();
-    if (it == 0) {
-      // Q fragments of this warp (rows w*16 .. w*16+15)
+    // the 64-position tile in two halves of 32 (keeps the score fragment small)
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+      const int q0 = p0 + 32 * half;
+      if (q0 >= hi) break;
+      // S = Q K^T (16 x 32)
+      float s[4][4];
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
-        const int r = w * 16 + (lane & 15);
-        const int c = ks * 2 + (lane >> 4);
-        ldsm_x4(smem_u32(sQ + tile_off<D>(r, c)), qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
+        uint32_t qa[4];  // Q fragment of this warp (rows w*16 .. w*16+15), K-step ks
+        {
+          const int r = w * 16 + (lane & 15);
+          const int c = ks * 2 + (lane >> 4);
+          ldsm_x4(smem_u32(sQ + tile_off<D>(r, c)), qa[0], qa[1], qa[2], qa[3]);
+        }
+#pragma unroll
+        for (int np = 0; np < 2; ++np) {  // pairs of 8-position tiles
+          const int r = 32 * half + np * 16 + (lane & 7) + ((lane >> 4) << 3);
+          const int c = ks * 2 + ((lane >> 3) & 1);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(smem_u32(sK[buf] + tile_off<D>(r, c)), b0, b1, b2, b3);
+          mma16816(s[2 * np], qa, b0, b1);
+          mma16816(s[2 * np + 1], qa, b2, b3);
+        }
       }
-    }
-    // S = Q K^T (16 x 64)
-    float s[8][4];
+      // mask + online softmax (log2 domain)
+      float mx[2] = {mrow[0], mrow[1]};
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+      for (int nt = 0; nt < 4; ++nt) {
 #pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {  // pairs of 8-position tiles
-        const int r = np * 16 + (lane & 7) + ((lane >> 4) << 3);
-        const int c = ks * 2 + ((lane >> 3) & 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(smem_u32(sK[buf] + tile_off<D>(r, c)), b0, b1, b2, b3);
-        mma16816(s[2 * np], qa[ks], b0, b1);
-        mma16816(s[2 * np + 1], qa[ks], b2, b3);
+        for (int e = 0; e < 4; ++e) {
+          const int j = q0 + nt * 8 + 2 * (lane & 3) + (e & 1);
+          const int rr = e >> 1;
+          const int pq = posq[rr];
+          const bool vis = j < hi && j <= pq && (P.window == 0 || pq - j < P.window);
+          const float v = vis ? s[nt][e] * sl2 : -INFINITY;
+          s[nt][e] = v;
+          mx[rr] = fmaxf(mx[rr], v);
+        }
       }
-    }
-    // mask + online softmax
-    float mx[2] = {mrow[0], mrow[1]};
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int j = p0 + nt * 8 + 2 * (lane & 3) + (e & 1);
-        const int rr = e >> 1;
-        const int pq = posq[rr];
-        const bool vis = j < hi && j <= pq && (P.window == 0 || pq - j < P.window);
-        const float v = vis ? s[nt][e] * sl2 : -INFINITY;
-        s[nt][e] = v;
-        mx[rr] = fmaxf(mx[rr], v);
+      for (int rr = 0; rr < 2; ++rr) {
+        mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
+        mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
       }
-    }
+      float alpha[2], base[2];
 #pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-      mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
-      mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
-    }
-    float alpha[2], base[2];
+      for (int rr = 0; rr < 2; ++rr) {
+        base[rr] = mx[rr] == -INFINITY ? 0.f : mx[rr];
+        alpha[rr] = mrow[rr] == -INFINITY ? 0.f : exp2f(mrow[rr] - base[rr]);
+        if (mx[rr] == -INFINITY) alpha[rr] = 1.f;
+        mrow[rr] = mx[rr];
+        lrow[rr] *= alpha[rr];
+      }
 #pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-      base[rr] = mx[rr] == -INFINITY ? 0.f : mx[rr];
-      alpha[rr] = mrow[rr] == -INFINITY ? 0.f : exp2f(mrow[rr] - base[rr]);
-      if (mx[rr] == -INFINITY) alpha[rr] = 1.f;
-      mrow[rr] = mx[rr];
-      lrow[rr] *= alpha[rr];
-    }
+      for (int i = 0; i < D / 8; ++i) {
+        o[i][0] *= alpha[0];
+        o[i][1] *= alpha[0];
+        o[i][2] *= alpha[1];
+        o[i][3] *= alpha[1];
+      }
+      // P V over 2 K-steps of 16 positions.  P (as A fragments) is split into
+      // a bf16 high part and the bf16 rounding of the remainder, so that P V
+      // is accumulated from a ~16-bit-mantissa P rather than bf16's 8 bits.
 #pragma unroll
-    for (int i = 0; i < D / 8; ++i) {
-      o[i][0] *= alpha[0];
-      o[i][1] *= alpha[0];
-      o[i][2] *= alpha[1];
-      o[i][3] *= alpha[1];
-    }
-    // P as A fragments (4 k16 steps over 64 positions), split into a bf16
-    // high part and the bf16 rounding of the remainder, so that P V is
-    // accumulated from a ~16-bit-mantissa P rather than bf16's 8 bits.
-    uint32_t pa[4][4], pl[4][4];
+      for (int kk = 0; kk < 2; ++kk) {
+        uint32_t pa[4], pl[4];
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      const float p0v = exp2f(s[nt][0] - base[0]), p1v = exp2f(s[nt][1] - base[0]);
-      const float p2v = exp2f(s[nt][2] - base[1]), p3v = exp2f(s[nt][3] - base[1]);
-      lrow[0] += p0v + p1v;
-      lrow[1] += p2v + p3v;
-      const int kk = nt >> 1, hi8 = nt & 1;
-      const float h0 = round_bf(p0v), h1 = round_bf(p1v), h2 = round_bf(p2v), h3 = round_bf(p3v);
-      pa[kk][hi8 * 2 + 0] = pack_bf16(h0, h1);
-      pa[kk][hi8 * 2 + 1] = pack_bf16(h2, h3);
-      pl[kk][hi8 * 2 + 0] = pack_bf16(p0v - h0, p1v - h1);
-      pl[kk][hi8 * 2 + 1] = pack_bf16(p2v - h2, p3v - h3);
-    }
-    // O += P V
+        for (int hi8 = 0; hi8 < 2; ++hi8) {
+          const int nt = 2 * kk + hi8;
+          const float p0v = exp2f(s[nt][0] - base[0]), p1v = exp2f(s[nt][1] - base[0]);
+          const float p2v = exp2f(s[nt][2] - base[1]), p3v = exp2f(s[nt][3] - base[1]);
+          lrow[0] += p0v + p1v;
+          lrow[1] += p2v + p3v;
+          const float h0 = round_bf(p0v), h1 = round_bf(p1v), h2 = round_bf(p2v), h3 = round_bf(p3v);
+          pa[hi8 * 2 + 0] = pack_bf16(h0, h1);
+          pa[hi8 * 2 + 1] = pack_bf16(h2, h3);
+          pl[hi8 * 2 + 0] = pack_bf16(p0v - h0, p1v - h1);
+          pl[hi8 * 2 + 1] = pack_bf16(p2v - h2, p3v - h3);
+        }
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-      for (int dp = 0; dp < D / 16; ++dp) {  // pairs of 8-wide d tiles
-        const int r = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-        const int c = dp * 2 + (lane >> 4);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(smem_u32(sV[buf] + tile_off<D>(r, c)), b0, b1, b2, b3);
-        mma16816(o[2 * dp], pa[kk], b0, b1);
-        mma16816(o[2 * dp + 1], pa[kk], b2, b3);
-        mma16816(o[2 * dp], pl[kk], b0, b1);
-        mma16816(o[2 * dp + 1], pl[kk], b2, b3);
+        for (int dp = 0; dp < D / 16; ++dp) {  // pairs of 8-wide d tiles
+          const int r = 32 * half + kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+          const int c = dp * 2 + (lane >> 4);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(smem_u32(sV[buf] + tile_off<D>(r, c)), b0, b1, b2, b3);
+          mma16816(o[2 * dp], pa, b0, b1);
+          mma16816(o[2 * dp + 1], pa, b2, b3);
+          mma16816(o[2 * dp], pl, b0, b1);
+          mma16816(o[2 * dp + 1], pl, b2, b3);
+        }
       }
     }
     epi_sync();
@@ -1394,7 +1401,7 @@ MK_DEV bool epi_wait(const LayerParams& P, const Smem& S, int id, uint32_t targe
 
 MK_DEV void run_epilogue(const LayerParams& P, const Smem& S, uint32_t epoch) {
   Misc* m = S.m;
-  const int et = threadIdx.x - 128;  // 0..127
+  const int et = threadIdx.x - kEpiBase;  // 0..127
   const uint32_t target = grid_target(P, epoch);
   uint32_t acc_ph[2] = {0, 0}, ucount = 0;
   bool ok = true;
@@ -1526,11 +1533,11 @@ __global__ void __launch_bounds__(kThreads, 1) mk_layer_kernel(const __grid_cons
     named_bar(3, kThreads - 32);
     if (threadIdx.x == 32) stamp(P, PH_COUNT, 1);
     const uint32_t epoch = m->epoch;
-    if (warp == 1) {
-      if (lane_id() < 4) run_mma(P, S);
-    } else if (warp < 4) {
+    if (warp >= 1 && warp <= 4) {
+      if (lane_id() == 0) run_mma(P, S);
+    } else if (warp == 5 || warp == 6) {
       run_stager(P, S, epoch);
-    } else {
+    } else if (warp >= 8) {
       run_epilogue(P, S, epoch);
     }
   }

@@ -7,7 +7,7 @@
 
 namespace mk {
 
-constexpr int kThreads = 256;     // 8 warps: TMA, MMA, 2 stagers, 4 epilogue/math
+constexpr int kThreads = 384;     // 12 warps: TMA, 4 MMA issuers, 2 stagers, spare, 4 epilogue/math
 constexpr int kStages = 7;        // weight ring depth (16 KB tile + 2 KB scales)
 constexpr int kKC = 512;          // K elements per split-K unit (bf16 phases)
 constexpr int kMaxT = 16;         // verify tokens per step (MMA N)
