@@ -216,6 +216,36 @@ mk_status mk_layer_get_info(mk_layer* layer, mk_layer_info* info);
  * the layer is destroyed.  Synchronous. */
 mk_status mk_get_timestamps(mk_layer* layer, uint64_t* host_buf, size_t n);
 
+/* One decode step of one layer, like mk_layer_create + mk_decode_step, but
+ * allocating nothing: for callers that cannot call cudaMalloc -- code that
+ * runs where device allocation is not allowed or not wanted, such as a
+ * process whose device memory is handed out by another allocator or pool, or
+ * one that must not grow its footprint after start-up.  (The pages describe
+ * no counterpart; this is an addition of this library.)
+ *
+ * Every library-owned buffer of the step -- split-K and attention partials,
+ * intermediates, counters, the repacked NVFP4 scale factors -- is carved out
+ * of one static device array of 16 MiB that every GPU loading the library
+ * holds until the process exits.  The caller still passes the weights, KV
+ * caches, inputs and outputs, exactly as for mk_layer_create/mk_decode_step.
+ * Layers whose buffers do not fit (roughly: small shapes such as hidden 256
+ * with 16 small experts fit; the 4096-hidden, 256-expert shapes do not) are
+ * rejected with MK_ERR_UNSUPPORTED before anything is launched (with
+ * MK_LOG=1 a line on stderr says why); the attention split uses at most 32
+ * chunks per KV head.
+ *
+ * The first call on a device performs a one-time set-up with that device
+ * current (it looks up the array's device address); make that first call
+ * before any stream capture.  The call is asynchronous on `stream`; every
+ * call re-zeroes the counters it needs and re-derives the scale factors, and
+ * all calls share the one array, so calls whose work overlaps on the GPU
+ * (other streams, other threads) race and give undefined results.  A
+ * device-side wait timeout leaves the outputs undefined and is not reported
+ * by this call.  Same argument rules and errors as mk_layer_create and
+ * mk_decode_step. */
+mk_status mk_decode_step_noalloc(const mk_layer_config* cfg, const mk_layer_weights* w,
+                                 const mk_step_io* io, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

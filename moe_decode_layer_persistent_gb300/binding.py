@@ -112,7 +112,11 @@ _lib_mk_selftest_stream = _sig("mk_selftest_stream", _c.c_int,
 _lib_mk_selftest_issue = _sig("mk_selftest_issue", _c.c_int,
                               [_c.c_int32, _c.c_int32, _c.POINTER(_c.c_longlong)])
 
-EXPORTED = ["mk_layer_create", "mk_decode_step", "mk_layer_status", "mk_layer_clear_status",
+_lib_mk_decode_step_noalloc = _sig("mk_decode_step_noalloc", _c.c_int,
+                                   [_c.POINTER(mk_layer_config), _c.POINTER(mk_layer_weights),
+                                    _c.POINTER(mk_step_io), _vp])
+
+EXPORTED = ["mk_layer_create", "mk_decode_step", "mk_decode_step_noalloc", "mk_layer_status", "mk_layer_clear_status",
             "mk_layer_destroy", "mk_stack_create", "mk_stack_step", "mk_stack_status",
             "mk_stack_destroy", "mk_status_string", "mk_layer_get_info", "mk_get_timestamps",
             "mk_selftest_quantize", "mk_selftest_mma", "mk_selftest_copy_scratch",
@@ -190,6 +194,16 @@ def make_step_io(T, ctx, x_in, x_out, k_cache, v_cache, q_in=None, next_k_cache=
 
 def mk_decode_step(layer, io, stream=None):
     _check("mk_decode_step", _lib_mk_decode_step(layer, ctypes.byref(io), _stream(stream)))
+
+
+def mk_decode_step_noalloc(cfg, weights, io, stream=None):
+    """One decode step without any device allocation (scratch in the
+    library's fixed static array; small layers only)."""
+    w = mk_layer_weights()
+    for n in _WEIGHT_FIELDS:
+        setattr(w, n, _ptr(weights.get(n)))
+    _check("mk_decode_step_noalloc", _lib_mk_decode_step_noalloc(
+        ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(io), _stream(stream)))
 
 
 def mk_layer_status(layer):

@@ -3,6 +3,7 @@
 // layer; a stack chains them with programmatic dependent launch).
 #include <algorithm>
 #include <cstdlib>
+#include <mutex>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -527,3 +528,225 @@ void mk_stack_destroy(mk_stack* S) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// mk_decode_step_noalloc: one decode step of a small layer for callers that
+// may not allocate device memory at all -- code that runs where cudaMalloc is
+// not allowed or not wanted (for example a host whose device memory is owned
+// by another allocator or pool, or a process that has finished its start-up
+// allocations).  Every library-owned buffer of the step (split-K partials,
+// attention partials, intermediates, counters, the repacked NVFP4 scale
+// factors) comes from the one fixed-size device array below, which every GPU
+// that loads the library holds until the process exits.
+namespace {
+
+constexpr size_t kNoAllocBytes = 16u << 20;   // 16 MiB
+constexpr int kNoAllocMaxChunks = 32;         // attention chunks per KV head
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocBytes];
+
+struct NoAllocDevice {
+  bool ready = false;
+  uint8_t* base = nullptr;  // device address of g_noalloc_scratch on this device
+  int sm_count = 0;
+};
+constexpr int kNoAllocMaxDevices = 64;
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+std::mutex g_noalloc_mutex;
+
+// Carves 256-byte-aligned pieces out of the scratch array (no allocation).
+struct Carve {
+  uint8_t* base;
+  size_t used = 0;
+  bool overflow = false;
+  template <class T>
+  T* take(size_t count) {
+    const size_t bytes = (std::max<size_t>(count * sizeof(T), 16) + 255) & ~static_cast<size_t>(255);
+    if (used + bytes > kNoAllocBytes) {
+      overflow = true;
+      return nullptr;
+    }
+    T* p = reinterpret_cast<T*>(base + used);
+    used += bytes;
+    return p;
+  }
+};
+
+}  // namespace
+
+extern "C" mk_status mk_decode_step_noalloc(const mk_layer_config* cfg, const mk_layer_weights* w,
+                                            const mk_step_io* io, void* stream) {
+  mk_status st = validate_config(cfg, w);
+  if (st != MK_OK) return st;
+  if (!io) return MK_ERR_INVALID_ARG;
+  int dev = -1;
+  MK_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return MK_ERR_UNSUPPORTED;
+  NoAllocDevice& D = g_noalloc_dev[dev];
+  {
+    // set-up, once per device, with that device current
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!D.ready) {
+      cudaDeviceProp prop;
+      MK_CUDA_TRY(cudaGetDeviceProperties(&prop, dev));
+      if (prop.major != 10 || prop.minor != 3) return MK_ERR_UNSUPPORTED;
+      void* p = nullptr;
+      MK_CUDA_TRY(cudaGetSymbolAddress(&p, g_noalloc_scratch));
+      MK_CUDA_TRY(cudaFuncSetAttribute(layer_kernel_ptr(), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       layer_smem_bytes()));
+      D.base = static_cast<uint8_t*>(p);
+      D.sm_count = prop.multiProcessorCount;
+      D.ready = true;
+    }
+  }
+  // the layer object of mk_layer_create, assembled on the stack
+  mk_layer L;
+  L.cfg = *cfg;
+  L.w = *w;
+  L.device = dev;
+  // the attention split targets sm_count / Hkv chunks per KV head; capping it
+  // keeps the chunk partials inside the fixed scratch (the grid stays one CTA
+  // per SM: P.grid below)
+  L.sm_count = std::min(D.sm_count, kNoAllocMaxChunks * std::max(1, cfg->n_kv_heads));
+  if (L.cfg.rms_eps == 0.f) L.cfg.rms_eps = 1e-6f;
+  if (L.cfg.wait_timeout_ns == 0) L.cfg.wait_timeout_ns = 200ull * 1000 * 1000;
+  const mk_layer_config& c = L.cfg;
+  LayerParams& P = L.tmpl;
+  std::memset(&P, 0, sizeof(P));
+  P.H = c.hidden;
+  P.Hq = c.n_q_heads;
+  P.Hkv = c.n_kv_heads;
+  P.d = c.head_dim;
+  P.window = c.window;
+  P.moe = c.ffn_kind == MK_FFN_MOE_NVFP4;
+  P.E = P.moe ? c.n_experts : 0;
+  P.topk = P.moe ? c.top_k : 0;
+  P.P = P.moe ? c.pooled_dim : 0;
+  P.I = P.moe ? c.expert_inter : 0;
+  P.F = P.moe ? 0 : c.dense_inter;
+  P.first_layer = (c.flags & MK_FIRST_LAYER) != 0;
+  P.fuse_next = (c.flags & MK_FUSE_NEXT_QKV) != 0;
+  P.renorm = (c.flags & MK_TOPK_RENORM) != 0;
+  P.Nqkv = P.Hq * P.d + 2 * P.Hkv * P.d;
+  P.eps = c.rms_eps;
+  P.timeout_ns = c.wait_timeout_ns;
+  P.grid = D.sm_count;
+  P.attn_norm_w = static_cast<const __nv_bfloat16*>(w->attn_norm_w);
+  P.ffn_norm_w = static_cast<const __nv_bfloat16*>(w->ffn_norm_w);
+  P.next_attn_norm_w = static_cast<const __nv_bfloat16*>(w->next_attn_norm_w);
+  P.ks_qkv = choose_ksplit(P.H);
+  P.tiles_qkv = (P.Nqkv + 127) / 128;
+  P.ks_o = choose_ksplit(P.Hq * P.d);
+  P.tiles_o = P.H / 128;
+  P.ks_rp = choose_ksplit(P.H);
+  if (P.moe) {
+    P.tiles_router = (P.E + 127) / 128;
+    P.tiles_pool = P.P / 128;
+    P.ks_unpool = choose_ksplit(P.P);
+    P.tiles_unpool = P.H / 128;
+  } else {
+    P.ks_dgu = choose_ksplit(P.H);
+    P.tiles_dgu = P.F / 128;
+    P.ks_ddown = choose_ksplit(P.F);
+    P.tiles_ddown = P.H / 128;
+  }
+  if (P.tiles_qkv > 256 || P.tiles_o > 256 || P.tiles_dgu > 256 ||
+      P.tiles_router + P.tiles_pool > 256)
+    return MK_ERR_UNSUPPORTED;
+  const int qd = P.Hq * P.d;
+  if (P.first_layer) {
+    st = encode_tmap_2d(&P.tm_qkv, w->w_qkv, 2, P.H, P.Nqkv, 64, 128);
+    if (st != MK_OK) return st;
+  }
+  st = encode_tmap_2d(&P.tm_o, w->w_o, 2, qd, P.H, 64, 128);
+  if (st == MK_OK && P.fuse_next) st = encode_tmap_2d(&P.tm_nqkv, w->next_w_qkv, 2, P.H, P.Nqkv, 64, 128);
+  if (st == MK_OK && P.moe) {
+    st = encode_tmap_2d(&P.tm_router, w->w_router, 2, P.H, P.E, 64, 128);
+    if (st == MK_OK) st = encode_tmap_2d(&P.tm_pool, w->w_pool, 2, P.H, P.P, 64, 128);
+    if (st == MK_OK) st = encode_tmap_2d(&P.tm_unpool, w->w_unpool, 2, P.P, P.H, 64, 128);
+    if (st == MK_OK)
+      st = encode_tmap_2d(&P.tm_gate, w->exp_gate_q, 1, P.P / 2, static_cast<uint64_t>(P.E) * P.I, 128, 128);
+    if (st == MK_OK)
+      st = encode_tmap_2d(&P.tm_up, w->exp_up_q, 1, P.P / 2, static_cast<uint64_t>(P.E) * P.I, 128, 128);
+    if (st == MK_OK)
+      st = encode_tmap_2d(&P.tm_down, w->exp_down_q, 1, P.I / 2, static_cast<uint64_t>(P.E) * P.P, 128, 128);
+    P.ts_gate = w->exp_gate_ts;
+    P.ts_up = w->exp_up_ts;
+    P.ts_down = w->exp_down_ts;
+  } else if (st == MK_OK) {
+    st = encode_tmap_2d(&P.tm_gate, w->w_gate, 2, P.H, P.F, 64, 128);
+    if (st == MK_OK) st = encode_tmap_2d(&P.tm_up, w->w_up, 2, P.H, P.F, 64, 128);
+    if (st == MK_OK) st = encode_tmap_2d(&P.tm_down, w->w_down, 2, P.F, P.H, 64, 128);
+  }
+  if (st != MK_OK) return st;
+
+  // every library-owned buffer, carved out of the scratch array
+  Carve cv{D.base};
+  const size_t T = kMaxT;
+  P.q_buf = cv.take<__nv_bfloat16>(T * qd);
+  P.o_buf = cv.take<__nv_bfloat16>(T * qd);
+  P.xmid = cv.take<__nv_bfloat16>(T * P.H);
+  P.ssq_mid = cv.take<float>(T * (P.H / 128));
+  P.ssq_out = cv.take<float>(T * (P.H / 128));
+  size_t part = static_cast<size_t>(P.ks_qkv) * T * P.tiles_qkv * 128;
+  part = std::max(part, static_cast<size_t>(P.ks_o) * T * P.tiles_o * 128);
+  size_t gu = 0, dn = 0;
+  if (P.moe) {
+    P.p_buf = cv.take<__nv_bfloat16>(T * P.P);
+    P.a_buf = cv.take<__nv_bfloat16>(T * P.topk * P.I);
+    P.z_buf = cv.take<__nv_bfloat16>(T * P.topk * P.P);
+    P.y_buf = cv.take<__nv_bfloat16>(T * P.P);
+    P.logits = cv.take<float>(T * kMaxE);
+    P.idx = cv.take<int32_t>(T * kMaxK);
+    P.wts = cv.take<float>(T * kMaxK);
+    P.pamax = cv.take<float>(T * (P.P / 128));
+    P.aamax = cv.take<float>(T * P.topk * (P.I / 128));
+    P.comb_ctr = cv.take<uint32_t>(T * (P.P / 128));
+    part = std::max(part, static_cast<size_t>(P.ks_rp) * T * (P.tiles_router + P.tiles_pool) * 128);
+    part = std::max(part, static_cast<size_t>(P.ks_unpool) * T * P.tiles_unpool * 128);
+    gu = sf_repacked_bytes(P.E, P.I, P.P);
+    dn = sf_repacked_bytes(P.E, P.P, P.I);
+    uint8_t* sf = cv.take<uint8_t>(2 * gu + dn);
+    P.sf_gate = sf;
+    P.sf_up = sf ? sf + gu : nullptr;
+    P.sf_down = sf ? sf + 2 * gu : nullptr;
+  } else {
+    P.a_buf = cv.take<__nv_bfloat16>(T * P.F);
+    part = std::max(part, static_cast<size_t>(P.ks_dgu) * 2 * T * P.tiles_dgu * 128);
+    part = std::max(part, static_cast<size_t>(P.ks_ddown) * T * P.tiles_ddown * 128);
+  }
+  P.part = cv.take<float>(part);
+  L.attn_max_chunks = std::min(kNoAllocMaxChunks, std::max(1, D.sm_count / P.Hkv));
+  P.attn_part = cv.take<float>(static_cast<size_t>(P.Hkv) * L.attn_max_chunks * 64 * (P.d + 2));
+  // counters that must start at zero each call: one contiguous block
+  uint32_t* zero = cv.take<uint32_t>(static_cast<size_t>(PH_COUNT) * 256 + 4 + kNumCounters + 2);
+  if (cv.overflow) {
+    if (log_enabled())
+      std::fprintf(stderr, "mk: mk_decode_step_noalloc: this layer needs more than the %zu-byte scratch\n",
+                   kNoAllocBytes);
+    return MK_ERR_UNSUPPORTED;
+  }
+  P.fix_ctr = zero;
+  P.misc_ctr = zero + PH_COUNT * 256;
+  P.bar_ctr = P.misc_ctr + 4;
+  P.epoch = P.bar_ctr + kNumCounters;
+  P.status = P.epoch + 1;
+  P.ts = nullptr;
+
+  // per-step fields and the attention split (same rules as mk_decode_step,
+  // with the chunk count capped for the fixed scratch)
+  LayerParams S;
+  st = fill_step(&L, io, S);
+  if (st != MK_OK) return st;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MK_CUDA_TRY(cudaMemsetAsync(zero, 0, (static_cast<size_t>(PH_COUNT) * 256 + 4 + kNumCounters + 2) * 4, s));
+  if (P.comb_ctr) MK_CUDA_TRY(cudaMemsetAsync(P.comb_ctr, 0, T * (P.P / 128) * 4, s));
+  if (P.moe) {
+    st = launch_sf_repack(w->exp_gate_s, const_cast<uint8_t*>(P.sf_gate), P.E, P.I, P.P, s);
+    if (st == MK_OK) st = launch_sf_repack(w->exp_up_s, const_cast<uint8_t*>(P.sf_up), P.E, P.I, P.P, s);
+    if (st == MK_OK) st = launch_sf_repack(w->exp_down_s, const_cast<uint8_t*>(P.sf_down), P.E, P.P, P.I, s);
+    if (st != MK_OK) return st;
+  }
+  return launch(&L, S, s, false);
+}
