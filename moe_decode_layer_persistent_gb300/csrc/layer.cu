@@ -56,7 +56,7 @@ struct Misc {
   uint64_t accempty[2];
   uint64_t route_ready;
   uint64_t mma_done;
-  uint64_t land[3];                // stager landing copies: [0] bf16 rows, [1..2] per-warp rows
+  uint64_t land[2][3];             // stager landing copies per operand buffer: [0] bf16 rows, [1..2] per-warp rows
   uint32_t tmem_base;
   uint32_t abort;
   uint32_t epoch;
@@ -74,6 +74,7 @@ struct Misc {
   int done_pairs[kMaxT * 16];      // epilogue: (token, tile) pairs this CTA completes
   int n_done;
   int grp_ok[4];                   // shared outcome of a group's wait: [0] stagers, [1] epilogue, [2..3] stager warps
+  uint32_t land_out[2][3];         // landing copies issued and not yet consumed (per buffer, slot)
 };
 static_assert(sizeof(Misc) <= 8192, "misc region");
 
@@ -548,25 +549,52 @@ MK_DEV void run_mma(const LayerParams& P, const Smem& S) {
 // ============================================================ stagers (warps 2-3)
 // Token operand of a bf16 unit.  The stager leader bulk-copies rows t < T of
 // src[t][k0 .. k0 + 64*nkb) (and the gain slice) into the landing area of the
-// operand buffer; then all stager threads write the swizzled operand, as
-// bf16(x * rnorm[t] * gain[k]) when a gain is given.  Rows >= T are zero.
-MK_DEV bool stage_bf16(const LayerParams& P, const Smem& S, uint8_t* bb, const __nv_bfloat16* src,
-                       int ld, int k0, int nkb, const __nv_bfloat16* gain, uint32_t& land_ph) {
+// operand buffer (issue_bf16, possibly one unit ahead); then all stager
+// threads write the swizzled operand, as bf16(x * rnorm[t] * gain[k]) when a
+// gain is given (stage_bf16).  Rows >= T are zero.
+struct BfSrc {
+  const __nv_bfloat16* src;
+  int ld;
+  const __nv_bfloat16* gain;
+};
+MK_DEV BfSrc bf_source(const LayerParams& P, int ph) {
+  switch (ph) {
+    case PH_QKV: return {P.x_in, P.H, P.attn_norm_w};
+    case PH_NQKV: return {P.x_out, P.H, P.next_attn_norm_w};
+    case PH_O: return {P.o_buf, P.Hq * P.d, nullptr};
+    case PH_RP: return {P.xmid, P.H, P.ffn_norm_w};
+    case PH_UNPOOL: return {P.y_buf, P.P, nullptr};
+    default: return {P.a_buf, P.F, nullptr};  // dense down
+  }
+}
+
+MK_DEV void issue_bf16(const LayerParams& P, const Smem& S, int ph, const Unit& U, int buf) {
+  const BfSrc src = bf_source(P, ph);
+  uint8_t* raw = S.bbuf(buf) + kLandOff;
+  uint8_t* graw = raw + kMaxT * U.nkb * 128;
+  const uint32_t rowbytes = static_cast<uint32_t>(U.nkb) * 128u;
+  const uint64_t pol = policy_evict_last();
+  uint64_t* lb = &S.m->land[buf][0];
+  S.m->land_out[buf][0] = 1;
+  mbar_arrive_expect_tx(lb, P.T * rowbytes + (src.gain ? rowbytes : 0u));
+  for (int t = 0; t < P.T; ++t)
+    bulk_load(raw + t * rowbytes, src.src + static_cast<size_t>(t) * src.ld + U.x0, rowbytes, lb, pol);
+  if (src.gain) bulk_load(graw, src.gain + U.x0, rowbytes, lb, pol);
+}
+
+MK_DEV bool stage_bf16(const LayerParams& P, const Smem& S, int ph, const Unit& U, int buf,
+                       uint32_t& land_ph) {
   const int tid = threadIdx.x - kStagerBase;
+  uint8_t* bb = S.bbuf(buf);
+  const int nkb = U.nkb;
+  const bool gain = bf_source(P, ph).gain != nullptr;
   uint8_t* raw = bb + kLandOff;
   uint8_t* graw = raw + kMaxT * nkb * 128;
   const uint32_t rowbytes = static_cast<uint32_t>(nkb) * 128u;
-  if (tid == 0) {
-    const uint64_t pol = policy_evict_last();
-    mbar_arrive_expect_tx(&S.m->land[0], P.T * rowbytes + (gain ? rowbytes : 0u));
-    for (int t = 0; t < P.T; ++t)
-      bulk_load(raw + t * rowbytes, src + static_cast<size_t>(t) * ld + k0, rowbytes, &S.m->land[0],
-                pol);
-    if (gain) bulk_load(graw, gain + k0, rowbytes, &S.m->land[0], pol);
-  }
-  if (!group_mbar_wait(P, S, &S.m->land[0], land_ph, ERR_TIMEOUT_B, tid == 0, kBarStage, 64, 0))
+  if (!group_mbar_wait(P, S, &S.m->land[buf][0], land_ph, ERR_TIMEOUT_B, tid == 0, kBarStage, 64, 0))
     return false;
   land_ph ^= 1;
+  if (tid == 0) S.m->land_out[buf][0] = 0;
   const int chunks = nkb * 8;  // 16-byte chunks per row
   for (int i = tid; i < kMaxT * chunks; i += 64) {
     const int t = i / chunks, c = i % chunks;
@@ -608,12 +636,7 @@ MK_DEV void quantize_row_given_srow(const __nv_bfloat16* row, int K, float s_row
     const float sbf = e4m3_to_float(sb);
     uint32_t w0 = 0, w1 = 0;
     if (sbf > 0.f) {
-      const float c = __fmul_rn(sbf, s_row);
-      float r[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) r[i] = __fdiv_rn(x[i], c);
-      w0 = cvt_e2m1x4(r[0], r[1], r[2], r[3]) | (cvt_e2m1x4(r[4], r[5], r[6], r[7]) << 16);
-      w1 = cvt_e2m1x4(r[8], r[9], r[10], r[11]) | (cvt_e2m1x4(r[12], r[13], r[14], r[15]) << 16);
+      e2m1_codes16(x, __fmul_rn(sbf, s_row), w0, w1);
     }
     sink.put(b, w0, w1, sb);
   }
@@ -621,14 +644,32 @@ MK_DEV void quantize_row_given_srow(const __nv_bfloat16* row, int K, float s_row
 
 // Token operand of an NVFP4 expert unit: row i = the i-th slot routed to the
 // expert, quantised from its bf16 row (p for gate/up, the SwiGLU output for
-// down), which each stager warp first bulk-copies into its own landing slot.
-MK_DEV bool stage_fp4(const LayerParams& P, const Smem& S, uint8_t* bb, const Unit& U, bool gu,
-                      uint32_t (&land_ph)[3]) {
+// down).  Stager warp w handles rows w, w+2, ...: each row is first
+// bulk-copied into the warp's landing slot of the operand buffer (the first
+// one by issue_fp4_row, possibly one unit ahead).
+MK_DEV const __nv_bfloat16* fp4_row(const LayerParams& P, const Smem& S, const Unit& U, bool gu, int i) {
+  const int s = S.m->slots[S.m->off[U.expert] + i];
+  return gu ? P.p_buf + static_cast<size_t>(s / P.topk) * P.P : P.a_buf + static_cast<size_t>(s) * P.I;
+}
+
+// Lane 0 of stager warp w: bulk-copy row i of unit U into the warp's slot.
+MK_DEV void issue_fp4_row(const LayerParams& P, const Smem& S, const Unit& U, bool gu, int i,
+                          int buf, int w) {
+  uint64_t* lb = &S.m->land[buf][1 + w];
+  const uint32_t rowbytes = static_cast<uint32_t>(U.K) * 2u;
+  S.m->land_out[buf][1 + w] = 1;
+  mbar_arrive_expect_tx(lb, rowbytes);
+  bulk_load(S.bbuf(buf) + kFp4LandOff + w * 4096, fp4_row(P, S, U, gu, i), rowbytes, lb,
+            policy_evict_last());
+}
+
+MK_DEV bool stage_fp4(const LayerParams& P, const Smem& S, const Unit& U, bool gu, int buf,
+                      bool first_issued, uint32_t (&land_ph)[2][3]) {
   Misc* m = S.m;
   const int warp = (threadIdx.x - kStagerBase) >> 5;  // 0..1
-  const int e = U.expert;
-  const int n = m->off[e + 1] - m->off[e];
+  const int n = m->off[U.expert + 1] - m->off[U.expert];
   const int K = U.K;
+  uint8_t* bb = S.bbuf(buf);
   // K-block padding beyond K must read as zero codes and zero scales
   if (K % 256) {
     const int tid = threadIdx.x - kStagerBase;
@@ -641,28 +682,38 @@ MK_DEV bool stage_fp4(const LayerParams& P, const Smem& S, uint8_t* bb, const Un
       bb[kBSfOff + (kb * 4 + (K % 256) / 64) * 512 + i] = 0;
   }
   uint8_t* slot = bb + kFp4LandOff + warp * 4096;
-  uint64_t* lb = &m->land[1 + warp];
-  const uint32_t rowbytes = static_cast<uint32_t>(K) * 2u;
+  uint64_t* lb = &m->land[buf][1 + warp];
   for (int i = warp; i < n; i += 2) {
-    const int s = m->slots[m->off[e] + i];
-    const int t = s / P.topk;
-    const __nv_bfloat16* row = gu ? P.p_buf + static_cast<size_t>(t) * P.P
-                                  : P.a_buf + static_cast<size_t>(s) * P.I;
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane_id() == 0) {
-      mbar_arrive_expect_tx(lb, rowbytes);
-      bulk_load(slot, row, rowbytes, lb, policy_evict_last());
+    if (i != warp || !first_issued) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane_id() == 0) issue_fp4_row(P, S, U, gu, i, buf, warp);
     }
     int wok = 0;
-    if (lane_id() == 0) wok = wait_bar(P, S, lb, land_ph[1 + warp], ERR_TIMEOUT_B) ? 1 : 0;
+    if (lane_id() == 0) wok = wait_bar(P, S, lb, land_ph[buf][1 + warp], ERR_TIMEOUT_B) ? 1 : 0;
     if (!__shfl_sync(0xffffffffu, wok, 0)) return false;
-    land_ph[1 + warp] ^= 1;
+    land_ph[buf][1 + warp] ^= 1;
+    if (lane_id() == 0) m->land_out[buf][1 + warp] = 0;
+    const int s = m->slots[m->off[U.expert] + i];
     OperandSink sink{bb, bb + kBSfOff, static_cast<uint32_t>(i)};
     quantize_row_given_srow(reinterpret_cast<const __nv_bfloat16*>(slot), K,
-                            gu ? m->srow_st[t] : m->srow_st[s], sink);
+                            gu ? m->srow_st[s / P.topk] : m->srow_st[s], sink);
   }
   return true;
+}
+
+// Prefetch of a unit's inputs into operand buffer `buf`'s landing area: the
+// bf16 rows by the stager leader, the first row of each stager warp for
+// NVFP4 units.  Returns whether anything was issued for the NVFP4 case.
+MK_DEV void prefetch_unit(const LayerParams& P, const Smem& S, int ph, const Unit& U, int buf) {
+  const int tid = threadIdx.x - kStagerBase;
+  if (!U.fp4) {
+    if (tid == 0) issue_bf16(P, S, ph, U, buf);
+    return;
+  }
+  const int w = tid >> 5;
+  const int n = S.m->off[U.expert + 1] - S.m->off[U.expert];
+  if (lane_id() == 0 && w < n) issue_fp4_row(P, S, U, ph == PH_GU, w, buf, w);
 }
 
 // RMSNorm factors of x_in (first layer), by the stager and epilogue warps: one row per warp at a
@@ -699,7 +750,7 @@ MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
   const int tid = threadIdx.x - kStagerBase;  // 0..63
   const int warp = tid >> 5;
   const uint32_t target = grid_target(P, epoch);
-  uint32_t b_ph[2] = {0, 0}, ucount = 0, land_ph[3] = {0, 0, 0};
+  uint32_t b_ph[2] = {0, 0}, ucount = 0, land_ph[2][3] = {{0, 0, 0}, {0, 0, 0}};
   bool ok = true;
   if (P.first_layer) rnorm_x_in(P, S);
   for (int ph = 0; ph < PH_COUNT && ok; ++ph) {
@@ -736,39 +787,24 @@ MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
     }
     stage_sync();
     const int n = phase_units(P, S, ph);
-    for (int u = first_unit(P, ph); u < n && ok; u += P.grid) {
+    const int u0 = first_unit(P, ph);
+    // the first unit's inputs; every later unit's were issued one unit ahead
+    if (u0 < n) prefetch_unit(P, S, ph, make_unit(P, S, ph, u0), ucount & 1);
+    for (int u = u0; u < n && ok; u += P.grid) {
       const Unit U = make_unit(P, S, ph, u);
       const uint32_t b = ucount & 1;
+      // the next unit's inputs go into the other buffer's landing area, which
+      // the MMA never reads (its previous contents were consumed last unit)
+      if (u + P.grid < n) prefetch_unit(P, S, ph, make_unit(P, S, ph, u + P.grid), b ^ 1);
       const uint64_t w0 = tnow(P);
       if (!group_mbar_wait(P, S, &m->bempty[b], b_ph[b] ^ 1, ERR_TIMEOUT_B, tid == 0, kBarStage, 64, 0)) {
         ok = false;
         break;
       }
       const uint64_t w1 = tnow(P);
-      uint8_t* bb = S.bbuf(b);
       bool sok = true;
-      switch (ph) {
-        case PH_QKV:
-          sok = stage_bf16(P, S, bb, P.x_in, P.H, U.x0, U.nkb, P.attn_norm_w, land_ph[0]);
-          break;
-        case PH_NQKV:
-          sok = stage_bf16(P, S, bb, P.x_out, P.H, U.x0, U.nkb, P.next_attn_norm_w, land_ph[0]);
-          break;
-        case PH_O:
-          sok = stage_bf16(P, S, bb, P.o_buf, P.Hq * P.d, U.x0, U.nkb, nullptr, land_ph[0]);
-          break;
-        case PH_RP:
-          sok = stage_bf16(P, S, bb, P.xmid, P.H, U.x0, U.nkb, P.ffn_norm_w, land_ph[0]);
-          break;
-        case PH_UNPOOL:
-          sok = stage_bf16(P, S, bb, P.y_buf, P.P, U.x0, U.nkb, nullptr, land_ph[0]);
-          break;
-        case PH_GU: sok = stage_fp4(P, S, bb, U, true, land_ph); break;
-        case PH_DOWN:
-          if (P.moe) sok = stage_fp4(P, S, bb, U, false, land_ph);
-          else sok = stage_bf16(P, S, bb, P.a_buf, P.F, U.x0, U.nkb, nullptr, land_ph[0]);
-          break;
-      }
+      if (U.fp4) sok = stage_fp4(P, S, U, ph == PH_GU, b, true, land_ph);
+      else sok = stage_bf16(P, S, ph, U, b, land_ph[b][0]);
       // both stager warps agree on the outcome before the next barrier
       if (lane_id() == 0) m->grp_ok[2 + warp] = sok ? 1 : 0;
       fence_proxy_async_smem();
@@ -788,9 +824,21 @@ MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
       ++ucount;
     }
   }
+  // landing copies still in flight (only after an abort) must land before exit
+  stage_sync();
+  if (lane_id() == 0) {
+    for (int i = 0; i < 6; ++i) {
+      const int buf = i / 3, sl = i % 3;
+      if (!(sl == 0 ? tid == 0 : warp == sl - 1) || !m->land_out[buf][sl]) continue;
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(&m->land[buf][sl], land_ph[buf][sl])) {
+        if (globaltimer() - t0 > P.timeout_ns) break;
+      }
+    }
+  }
 }
 
-// ============================================================ epilogue (warps 4-7)
+// ============================================================ epilogue (warps 8-11)
 // Cross-warp reduction over the 128 epilogue threads of 16 per-token values:
 // returns, in thread t (< 16), the sum (or max) for token t.
 template <bool kMax>
@@ -965,15 +1013,17 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
   const uint32_t taddr = m->tmem_base + (static_cast<uint32_t>(32 * q) << 16) + 128 * b;
   float g[kMaxT], u[kMaxT];
   // the four MMA lanes' partial sums (K-steps 0..3 of every K-block)
+  // the four MMA warps' partial sums (K-steps 0..3 of every K-block): all
+  // loads issued, one wait
   auto load_sum = [&](uint32_t col, float (&acc)[kMaxT]) {
-    tmem_ld16(col, acc);
-#pragma unroll 1
-    for (int l = 1; l < 4; ++l) {
-      float v[kMaxT];
-      tmem_ld16(col + 16 * l, v);
+    uint32_t r[4][16];
 #pragma unroll
-      for (int t = 0; t < kMaxT; ++t) acc[t] += v[t];
-    }
+    for (int l = 0; l < 4; ++l) tmem_ld16_nowait(col + 16 * l, r[l]);
+    tmem_ld_wait();
+#pragma unroll
+    for (int t = 0; t < kMaxT; ++t)
+      acc[t] = (__uint_as_float(r[0][t]) + __uint_as_float(r[1][t])) +
+               (__uint_as_float(r[2][t]) + __uint_as_float(r[3][t]));
   };
   load_sum(taddr, g);
   if (U.pair == 2) load_sum(taddr + 64, u);
@@ -1508,9 +1558,10 @@ __global__ void __launch_bounds__(kThreads, 1) mk_layer_kernel(const __grid_cons
     }
     mbar_init(&m->route_ready, 1);
     mbar_init(&m->mma_done, 4);
-    for (int i = 0; i < 3; ++i) mbar_init(&m->land[i], 1);
+    for (int i = 0; i < 6; ++i) mbar_init(&m->land[i / 3][i % 3], 1);
     m->abort = 0;
     m->n_act = 0;
+    for (int i = 0; i < 6; ++i) m->land_out[i / 3][i % 3] = 0;
     fence_mbar_init();
   }
   if (warp == 1) {

@@ -54,6 +54,38 @@ MK_DEV void load_bf16x16(const __nv_bfloat16* p, float (&x)[16]) {
   }
 }
 
+// E2M1 codes (two packed words, element 0 in the low nibble) of the
+// correctly rounded quotients x_i / c, without sixteen divisions: with
+// rc = 1/c rounded, x_i * rc lies within 2 ulp of the rounded quotient, so the
+// interval r(1 - 2^-20) .. r(1 + 2^-20) holds it.  Rounding to E2M1 is
+// monotone, so when both ends of every interval give the same codes those are
+// the quotients' codes; otherwise (a quotient near a rounding boundary, or
+// 1/c out of range) the sixteen exact divisions decide.
+MK_DEV void e2m1_codes16(const float (&x)[16], float c, uint32_t& w0, uint32_t& w1) {
+  const float rc = __frcp_rn(c);
+  float lo[16], hi[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float r = __fmul_rn(x[i], rc);
+    lo[i] = __fmul_rn(r, 0.99999904632568359375f);   // 1 - 2^-20
+    hi[i] = __fmul_rn(r, 1.00000095367431640625f);   // 1 + 2^-20
+  }
+  const uint32_t l0 = cvt_e2m1x4(lo[0], lo[1], lo[2], lo[3]) | (cvt_e2m1x4(lo[4], lo[5], lo[6], lo[7]) << 16);
+  const uint32_t l1 = cvt_e2m1x4(lo[8], lo[9], lo[10], lo[11]) | (cvt_e2m1x4(lo[12], lo[13], lo[14], lo[15]) << 16);
+  const uint32_t h0 = cvt_e2m1x4(hi[0], hi[1], hi[2], hi[3]) | (cvt_e2m1x4(hi[4], hi[5], hi[6], hi[7]) << 16);
+  const uint32_t h1 = cvt_e2m1x4(hi[8], hi[9], hi[10], hi[11]) | (cvt_e2m1x4(hi[12], hi[13], hi[14], hi[15]) << 16);
+  if (l0 == h0 && l1 == h1 && rc < 3.0e38f) {
+    w0 = l0;
+    w1 = l1;
+    return;
+  }
+  float r[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) r[i] = __fdiv_rn(x[i], c);
+  w0 = cvt_e2m1x4(r[0], r[1], r[2], r[3]) | (cvt_e2m1x4(r[4], r[5], r[6], r[7]) << 16);
+  w1 = cvt_e2m1x4(r[8], r[9], r[10], r[11]) | (cvt_e2m1x4(r[12], r[13], r[14], r[15]) << 16);
+}
+
 // One warp quantises one row of K bf16 values (K % 16 == 0, row 16-byte
 // aligned).  For every 16-element block b the sink receives the 8 code bytes
 // (two 32-bit words, element 16b in the low nibble of the first byte) and the
@@ -82,12 +114,7 @@ MK_DEV float quantize_row_nvfp4(const __nv_bfloat16* row, int K, Sink& sink) {
     const float sbf = e4m3_to_float(sb);
     uint32_t w0 = 0, w1 = 0;
     if (sbf > 0.f) {
-      const float c = __fmul_rn(sbf, s_row);
-      float r[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) r[i] = __fdiv_rn(x[i], c);
-      w0 = cvt_e2m1x4(r[0], r[1], r[2], r[3]) | (cvt_e2m1x4(r[4], r[5], r[6], r[7]) << 16);
-      w1 = cvt_e2m1x4(r[8], r[9], r[10], r[11]) | (cvt_e2m1x4(r[12], r[13], r[14], r[15]) << 16);
+      e2m1_codes16(x, __fmul_rn(sbf, s_row), w0, w1);
     }
     sink.put(b, w0, w1, sb);
   }
