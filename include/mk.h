@@ -210,10 +210,12 @@ mk_status mk_layer_get_info(mk_layer* layer, mk_layer_info* info);
  * (producer waiting for a free stage, MMA waiting for weights, for the token
  * operand, for a free accumulator, stager waiting for a free operand buffer,
  * stager working, epilogue waiting for an accumulator, epilogue working,
- * MMA issuing);
- * row 9 starts with (kernel start, inputs ready, kernel end).  Stamps of
- * unused phases read 0; the nanosecond slots accumulate across steps until
- * the layer is destroyed.  Synchronous. */
+ * MMA issuing) and three more stamps (MMA starts the phase's units, stagers'
+ * input dependency met, epilogue starts the phase's units);
+ * row 9 starts with (kernel start, inputs ready, kernel end, router top-k
+ * start, routing released).  All values are of the last step; stamps of
+ * unused phases read 0.  Each CTA keeps them in shared memory and writes them
+ * out when it exits, so that timing costs little.  Synchronous. */
 mk_status mk_get_timestamps(mk_layer* layer, uint64_t* host_buf, size_t n);
 
 /* One decode step of one layer, like mk_layer_create + mk_decode_step, but

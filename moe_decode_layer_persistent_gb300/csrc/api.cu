@@ -324,6 +324,8 @@ mk_status mk_layer_create(const mk_layer_config* cfg, const mk_layer_weights* w,
     MK_TRY(dalloc(L, &P.pamax, T * (P.P / 128)));
     MK_TRY(dalloc(L, &P.aamax, T * P.topk * (P.I / 128)));
     MK_TRY(dalloc(L, &P.comb_ctr, T * (P.P / 128)));
+    MK_TRY(dalloc(L, &P.exp_sync, 2 * kMaxE));
+    MK_TRY(dalloc(L, &P.srow_a, T * kMaxK));
     part = std::max(part, static_cast<size_t>(P.ks_rp) * T * (P.tiles_router + P.tiles_pool) * 128);
     part = std::max(part, static_cast<size_t>(P.ks_unpool) * T * P.tiles_unpool * 128);
     uint8_t* sf = nullptr;
@@ -347,6 +349,7 @@ mk_status mk_layer_create(const mk_layer_config* cfg, const mk_layer_weights* w,
                 static_cast<size_t>(P.Hkv) * L->attn_max_chunks * 64 * (P.d + 2)));
   MK_TRY(dalloc(L, &P.fix_ctr, static_cast<size_t>(PH_COUNT) * 256));
   MK_TRY(dalloc(L, &P.misc_ctr, 4));
+  MK_TRY(dalloc(L, &P.sched, PH_COUNT));
   MK_TRY(dalloc(L, &P.bar_ctr, kNumCounters));
   MK_TRY(dalloc(L, &P.epoch, 1));
   MK_TRY(dalloc(L, &P.status, 1));
@@ -387,8 +390,10 @@ mk_status mk_layer_clear_status(mk_layer* layer) {
   MK_CUDA_TRY(cudaMemset(P.bar_ctr, 0, kNumCounters * sizeof(uint32_t)));
   MK_CUDA_TRY(cudaMemset(P.fix_ctr, 0, PH_COUNT * 256 * sizeof(uint32_t)));
   MK_CUDA_TRY(cudaMemset(P.misc_ctr, 0, 4 * sizeof(uint32_t)));
+  MK_CUDA_TRY(cudaMemset(P.sched, 0, PH_COUNT * sizeof(uint32_t)));
   if (P.comb_ctr)
     MK_CUDA_TRY(cudaMemset(P.comb_ctr, 0, kMaxT * (P.P / 128) * sizeof(uint32_t)));
+  if (P.exp_sync) MK_CUDA_TRY(cudaMemset(P.exp_sync, 0, 2 * kMaxE * sizeof(uint32_t)));
   return MK_OK;
 }
 
@@ -702,6 +707,8 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_layer_config* cfg, const mk
     P.pamax = cv.take<float>(T * (P.P / 128));
     P.aamax = cv.take<float>(T * P.topk * (P.I / 128));
     P.comb_ctr = cv.take<uint32_t>(T * (P.P / 128));
+    P.exp_sync = cv.take<uint32_t>(2 * kMaxE);
+    P.srow_a = cv.take<float>(T * kMaxK);
     part = std::max(part, static_cast<size_t>(P.ks_rp) * T * (P.tiles_router + P.tiles_pool) * 128);
     part = std::max(part, static_cast<size_t>(P.ks_unpool) * T * P.tiles_unpool * 128);
     gu = sf_repacked_bytes(P.E, P.I, P.P);
@@ -719,7 +726,7 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_layer_config* cfg, const mk
   L.attn_max_chunks = std::min(kNoAllocMaxChunks, std::max(1, D.sm_count / P.Hkv));
   P.attn_part = cv.take<float>(static_cast<size_t>(P.Hkv) * L.attn_max_chunks * 64 * (P.d + 2));
   // counters that must start at zero each call: one contiguous block
-  uint32_t* zero = cv.take<uint32_t>(static_cast<size_t>(PH_COUNT) * 256 + 4 + kNumCounters + 2);
+  uint32_t* zero = cv.take<uint32_t>(static_cast<size_t>(PH_COUNT) * 256 + 4 + kNumCounters + 2 + PH_COUNT);
   if (cv.overflow) {
     if (log_enabled())
       std::fprintf(stderr, "mk: mk_decode_step_noalloc: this layer needs more than the %zu-byte scratch\n",
@@ -731,6 +738,7 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_layer_config* cfg, const mk
   P.bar_ctr = P.misc_ctr + 4;
   P.epoch = P.bar_ctr + kNumCounters;
   P.status = P.epoch + 1;
+  P.sched = P.status + 1;
   P.ts = nullptr;
 
   // per-step fields and the attention split (same rules as mk_decode_step,
@@ -740,8 +748,9 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_layer_config* cfg, const mk
   if (st != MK_OK) return st;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  MK_CUDA_TRY(cudaMemsetAsync(zero, 0, (static_cast<size_t>(PH_COUNT) * 256 + 4 + kNumCounters + 2) * 4, s));
+  MK_CUDA_TRY(cudaMemsetAsync(zero, 0, (static_cast<size_t>(PH_COUNT) * 256 + 4 + kNumCounters + 2 + PH_COUNT) * 4, s));
   if (P.comb_ctr) MK_CUDA_TRY(cudaMemsetAsync(P.comb_ctr, 0, T * (P.P / 128) * 4, s));
+  if (P.exp_sync) MK_CUDA_TRY(cudaMemsetAsync(P.exp_sync, 0, 2 * kMaxE * 4, s));
   if (P.moe) {
     st = launch_sf_repack(w->exp_gate_s, const_cast<uint8_t*>(P.sf_gate), P.E, P.I, P.P, s);
     if (st == MK_OK) st = launch_sf_repack(w->exp_up_s, const_cast<uint8_t*>(P.sf_up), P.E, P.I, P.P, s);

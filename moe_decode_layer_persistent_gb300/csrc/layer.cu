@@ -45,7 +45,8 @@ constexpr uint32_t kBSfOff = 16384;                          // scales inside a 
 constexpr uint32_t kLandOff = 16384;   // bf16 units: raw input rows (<= 16 KB), then the gain slice
 constexpr uint32_t kFp4LandOff = 32768; // NVFP4 units: two 4 KB row slots, one per stager warp
 constexpr uint32_t kOffMisc = kOffB + 2 * kBBufBytes;
-constexpr uint32_t kSmemBytes = kOffMisc + 8192 + 1024;     // + alignment slack
+constexpr uint32_t kOffTs = kOffMisc + 8192;                 // self-timing block
+constexpr uint32_t kSmemBytes = kOffTs + kTsPerCta * 8 + 1024;   // + alignment slack
 
 struct Misc {
   uint64_t full[kStages];
@@ -57,6 +58,8 @@ struct Misc {
   uint64_t route_ready;
   uint64_t mma_done;
   uint64_t land[2][3];             // stager landing copies per operand buffer: [0] bf16 rows, [1..2] per-warp rows
+  uint64_t uq_full[8];             // unit queue: slot written by the producer
+  uint64_t uq_empty[8];            // unit queue: slot read by the 4 MMA issuers, stager and epilogue leaders
   uint32_t tmem_base;
   uint32_t abort;
   uint32_t epoch;
@@ -74,6 +77,8 @@ struct Misc {
   int done_pairs[kMaxT * 16];      // epilogue: (token, tile) pairs this CTA completes
   int n_done;
   int grp_ok[4];                   // shared outcome of a group's wait: [0] stagers, [1] epilogue, [2..3] stager warps
+  int pref_ok[2];                  // stagers: a unit's first input rows were copied ahead (per buffer)
+  int uq[8];                       // unit queue: the CTA's next units in order, -1 ends a phase
   uint32_t land_out[2][3];         // landing copies issued and not yet consumed (per buffer, slot)
 };
 static_assert(sizeof(Misc) <= 8192, "misc region");
@@ -81,6 +86,7 @@ static_assert(sizeof(Misc) <= 8192, "misc region");
 struct Smem {
   uint8_t* base;
   Misc* m;
+  uint64_t* ts;  // self-timing block (used only when P.ts is set)
   MK_DEV uint8_t* a_tile(int s) const { return base + kOffA + s * kTileBytes; }
   MK_DEV uint8_t* sf(int s) const { return base + kOffSF + s * kSfBytes; }
   MK_DEV uint8_t* bbuf(int b) const { return base + kOffB + b * kBBufBytes; }
@@ -89,7 +95,8 @@ struct Smem {
 // ------------------------------------------------------------ errors / waits
 enum : uint32_t {
   ERR_TIMEOUT_FULL = 0x100, ERR_TIMEOUT_EMPTY = 0x200, ERR_TIMEOUT_B = 0x300,
-  ERR_TIMEOUT_ACC = 0x400, ERR_TIMEOUT_GRID = 0x500, ERR_TIMEOUT_ROUTE = 0x600
+  ERR_TIMEOUT_ACC = 0x400, ERR_TIMEOUT_GRID = 0x500, ERR_TIMEOUT_ROUTE = 0x600,
+  ERR_TIMEOUT_EXPERT = 0x700, ERR_TIMEOUT_QUEUE = 0x800
 };
 
 MK_DEV bool aborted(const LayerParams& P, const Smem& S) {
@@ -102,28 +109,29 @@ MK_DEV void raise_error(const LayerParams& P, const Smem& S, uint32_t code) {
 }
 
 // Bounded mbarrier wait: gives up on timeout or when the CTA/grid aborted.
+// The waiting thread sleeps in the barrier (woken when the phase completes)
+// and checks for an abort or a timeout about every microsecond.
 MK_DEV bool wait_bar(const LayerParams& P, const Smem& S, uint64_t* bar, uint32_t parity,
                      uint32_t code) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
-  uint32_t spins = 0;
-  while (!mbar_try_wait(bar, parity)) {
-    if ((++spins & 63u) == 0) {
-      if (aborted(P, S)) return false;
-      if (globaltimer() - t0 > P.timeout_ns) {
-        raise_error(P, S, code);
-        return false;
-      }
+  while (!mbar_try_wait_sleep(bar, parity, 1000u)) {
+    if (aborted(P, S)) return false;
+    if (globaltimer() - t0 > P.timeout_ns) {
+      raise_error(P, S, code);
+      return false;
     }
   }
   return true;
 }
 
-MK_DEV void stamp(const LayerParams& P, int ph, int slot) {
-  if (P.ts) P.ts[(static_cast<size_t>(blockIdx.x) * (PH_COUNT + 1) + ph) * kTsSlots + slot] = globaltimer();
+// Self-timing: each slot has one writer; the block is copied to P.ts when
+// the CTA exits, so that stamping costs a shared-memory access.
+MK_DEV void stamp(const LayerParams& P, const Smem& S, int ph, int slot) {
+  if (P.ts) S.ts[ph * kTsSlots + slot] = globaltimer();
 }
-MK_DEV void stamp_add(const LayerParams& P, int ph, int slot, uint64_t ns) {
-  if (P.ts) P.ts[(static_cast<size_t>(blockIdx.x) * (PH_COUNT + 1) + ph) * kTsSlots + slot] += ns;
+MK_DEV void stamp_add(const LayerParams& P, const Smem& S, int ph, int slot, uint64_t ns) {
+  if (P.ts) S.ts[ph * kTsSlots + slot] += ns;
 }
 // now() only when self-timing is on (0 otherwise)
 MK_DEV uint64_t tnow(const LayerParams& P) { return P.ts ? globaltimer() : 0; }
@@ -138,11 +146,32 @@ MK_DEV bool grid_wait(const LayerParams& P, const Smem& S, int id, uint32_t targ
   if (static_cast<int32_t>(ld_acquire(c) - target) >= 0) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
-    for (int i = 0; i < 32; ++i)
+    // short sleeps between polls leave the issue slots to working warps
+    for (int i = 0; i < 8; ++i) {
+      __nanosleep(100);
       if (static_cast<int32_t>(ld_acquire(c) - target) >= 0) return true;
+    }
     if (aborted(P, S)) return false;
     if (globaltimer() - t0 > P.timeout_ns) {
       raise_error(P, S, ERR_TIMEOUT_GRID | static_cast<uint32_t>(id << 4));
+      return false;
+    }
+  }
+}
+
+// One thread polls a flag holding the epoch + 1 of the launch that set it.
+MK_DEV bool flag_wait(const LayerParams& P, const Smem& S, const uint32_t* f, uint32_t value,
+                      uint32_t code) {
+  if (static_cast<int32_t>(ld_acquire(f) - value) >= 0) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    for (int i = 0; i < 8; ++i) {
+      __nanosleep(100);
+      if (static_cast<int32_t>(ld_acquire(f) - value) >= 0) return true;
+    }
+    if (aborted(P, S)) return false;
+    if (globaltimer() - t0 > P.timeout_ns) {
+      raise_error(P, S, code);
       return false;
     }
   }
@@ -171,6 +200,56 @@ MK_DEV bool group_grid_wait(const LayerParams& P, const Smem& S, int id, uint32_
   named_bar(bar_id, n);
   const bool ok = *reinterpret_cast<volatile int*>(&S.m->grp_ok[slot]) != 0;
   named_bar(bar_id, n);
+  return ok;
+}
+MK_DEV bool group_flag_wait(const LayerParams& P, const Smem& S, const uint32_t* f, uint32_t value,
+                            bool leader, int bar_id, int n, int slot) {
+  if (leader) S.m->grp_ok[slot] = flag_wait(P, S, f, value, ERR_TIMEOUT_EXPERT) ? 1 : 0;
+  named_bar(bar_id, n);
+  const bool ok = *reinterpret_cast<volatile int*>(&S.m->grp_ok[slot]) != 0;
+  named_bar(bar_id, n);
+  return ok;
+}
+
+// ------------------------------------------------------------ unit queue
+// The producer claims the CTA's units (statically in the launch's first weight
+// phase, so that it can stream before the previous launch ends; from a grid
+// counter in every later phase, so that faster CTAs take more units) and
+// hands them, in order, to the MMA issuers, the stagers and the epilogue
+// through a ring of kUQ slots; -1 ends a phase.
+constexpr int kUQ = 8;
+struct QCursor {
+  uint32_t slot = 0, par = 0;
+  MK_DEV void advance() {
+    if (++slot == kUQ) { slot = 0; par ^= 1; }
+  }
+};
+MK_DEV bool queue_push(const LayerParams& P, const Smem& S, QCursor& q, int v) {
+  if (!wait_bar(P, S, &S.m->uq_empty[q.slot], q.par ^ 1, ERR_TIMEOUT_QUEUE)) return false;
+  S.m->uq[q.slot] = v;
+  mbar_arrive(&S.m->uq_full[q.slot]);
+  q.advance();
+  return true;
+}
+// One thread (an MMA issuer).
+MK_DEV bool queue_pop1(const LayerParams& P, const Smem& S, QCursor& q, int& v) {
+  if (!wait_bar(P, S, &S.m->uq_full[q.slot], q.par, ERR_TIMEOUT_QUEUE)) return false;
+  v = *reinterpret_cast<volatile int*>(&S.m->uq[q.slot]);
+  mbar_arrive(&S.m->uq_empty[q.slot]);
+  q.advance();
+  return true;
+}
+// A named-barrier group (stagers or epilogue): the leader waits, everyone reads
+// the slot, then the leader frees it.
+MK_DEV bool queue_pop_group(const LayerParams& P, const Smem& S, QCursor& q, int& v, bool leader,
+                            int bar_id, int n, int slot) {
+  if (leader) S.m->grp_ok[slot] = wait_bar(P, S, &S.m->uq_full[q.slot], q.par, ERR_TIMEOUT_QUEUE) ? 1 : 0;
+  named_bar(bar_id, n);
+  const bool ok = *reinterpret_cast<volatile int*>(&S.m->grp_ok[slot]) != 0;
+  v = *reinterpret_cast<volatile int*>(&S.m->uq[q.slot]);
+  named_bar(bar_id, n);
+  if (ok && leader) mbar_arrive(&S.m->uq_empty[q.slot]);
+  q.advance();
   return ok;
 }
 constexpr int kBarEpi = 1;     // warps 4-7
@@ -231,7 +310,7 @@ MK_DEV int phase_dep(const LayerParams& P, int ph) {
     case PH_O: return BAR_MERGE;
     case PH_RP: return BAR_O;
     case PH_GU: return BAR_RP;
-    case PH_DOWN: return P.moe ? BAR_GU : BAR_RP;
+    case PH_DOWN: return P.moe ? -1 : BAR_RP;  // MoE: per expert (exp_sync)
     case PH_UNPOOL: return BAR_DOWN;
     case PH_NQKV: return BAR_X;
   }
@@ -422,27 +501,44 @@ MK_DEV void build_routing(const LayerParams& P, const Smem& S) {
 }
 
 // ============================================================ producer (warp 0)
+MK_DEV int first_gemm_phase(const LayerParams& P) { return P.first_layer ? PH_QKV : PH_O; }
+
 MK_DEV void run_producer(const LayerParams& P, const Smem& S) {
   Misc* m = S.m;
   const uint64_t pol = policy_evict_first();
   uint32_t stage = 0, phase = 0;
-  bool route_known = false;
+  QCursor q;
+  bool route_known = false, prev_done = false;
   bool ok = true;
+  const int ph0 = first_gemm_phase(P);
   for (int ph = 0; ph < PH_COUNT && ok; ++ph) {
     if (!phase_is_gemm(ph) || !phase_active(P, ph)) continue;
     if (P.moe && ph == PH_GU && !route_known) {
       if (!wait_bar(P, S, &m->route_ready, 0, ERR_TIMEOUT_ROUTE)) { ok = false; break; }
       route_known = true;
     }
+    // claimed units: the previous launch of this layer (which resets the
+    // counters at its end) must be complete
+    const bool claimed = ph != ph0;
+    if (claimed && !prev_done) {
+      pdl_wait();
+      prev_done = true;
+    }
     const int n = phase_units(P, S, ph);
-    for (int u = first_unit(P, ph); u < n && ok; u += P.grid) {
+    int u = first_unit(P, ph);
+    while (ok) {
+      if (claimed) u = static_cast<int>(atomicAdd(P.sched + ph, 1u));
+      const bool end = u >= n;
+      if (!queue_push(P, S, q, end ? -1 : u)) { ok = false; break; }
+      if (end) break;
       const Unit U = make_unit(P, S, ph, u);
+      if (!claimed) u += P.grid;
       const uint32_t bytes = kTileBytes + (U.fp4 ? kSfBytes : 0);
       for (int kb = 0; kb < U.nkb && ok; ++kb) {
         for (int j = 0; j < U.pair; ++j) {
           const uint64_t w0 = tnow(P);
           if (!wait_bar(P, S, &m->empty[stage], phase ^ 1, ERR_TIMEOUT_EMPTY)) { ok = false; break; }
-          if (P.ts) stamp_add(P, ph, 4, globaltimer() - w0);
+          if (P.ts) stamp_add(P, S, ph, 4, globaltimer() - w0);
           mbar_arrive_expect_tx(&m->full[stage], bytes);
           const int x = U.x0 + kb * (U.fp4 ? 128 : 64);
           tma_load_2d(S.a_tile(stage), U.map[j], &m->full[stage], x, U.row0, pol);
@@ -451,14 +547,14 @@ MK_DEV void run_producer(const LayerParams& P, const Smem& S) {
         }
       }
     }
-    stamp(P, ph, 3);
+    stamp(P, S, ph, 3);
   }
   // Drain: every issued copy must land before the CTA may exit.
   for (int s = 0; s < kStages; ++s) {
     // the most recent use of stage s had parity (phase ^ (s >= stage ? 1 : 0))
     const uint32_t par = s < static_cast<int>(stage) ? phase : phase ^ 1;
     const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(&m->full[s], par)) {
+    while (!mbar_try_wait_sleep(&m->full[s], par, 1000u)) {
       if (globaltimer() - t0 > P.timeout_ns) break;
     }
   }
@@ -480,6 +576,7 @@ MK_DEV void run_mma(const LayerParams& P, const Smem& S) {
   const uint32_t tbase = m->tmem_base;
   uint32_t stage = 0, phase = 0, acc_ph[2] = {0, 0}, b_ph[2] = {0, 0};
   uint32_t ucount = 0, sfreg = 0;
+  QCursor q;
   bool ok = true;
   bool route_known = false;
   for (int ph = 0; ph < PH_COUNT && ok; ++ph) {
@@ -488,8 +585,11 @@ MK_DEV void run_mma(const LayerParams& P, const Smem& S) {
       if (!wait_bar(P, S, &m->route_ready, 0, ERR_TIMEOUT_ROUTE)) { ok = false; break; }
       route_known = true;
     }
-    const int n = phase_units(P, S, ph);
-    for (int u = first_unit(P, ph); u < n && ok; u += P.grid) {
+    if (l == 0) stamp(P, S, ph, 13);
+    while (ok) {
+      int u;
+      if (!queue_pop1(P, S, q, u)) { ok = false; break; }
+      if (u < 0) break;
       const Unit U = make_unit(P, S, ph, u);
       const uint32_t b = ucount & 1;
       uint64_t w0 = tnow(P);
@@ -498,8 +598,8 @@ MK_DEV void run_mma(const LayerParams& P, const Smem& S) {
       if (!wait_bar(P, S, &m->bfull[b], b_ph[b], ERR_TIMEOUT_B)) { ok = false; break; }
       if (P.ts && l == 0) {
         const uint64_t w2 = globaltimer();
-        stamp_add(P, ph, 7, w1 - w0);
-        stamp_add(P, ph, 6, w2 - w1);
+        stamp_add(P, S, ph, 7, w1 - w0);
+        stamp_add(P, S, ph, 6, w2 - w1);
       }
       tc_fence_after();
       uint8_t* bb = S.bbuf(b);
@@ -508,7 +608,7 @@ MK_DEV void run_mma(const LayerParams& P, const Smem& S) {
           const uint64_t wf = tnow(P);
           if (!wait_bar(P, S, &m->full[stage], phase, ERR_TIMEOUT_FULL)) { ok = false; break; }
           const uint64_t wi = tnow(P);
-          if (P.ts && l == 0) stamp_add(P, ph, 5, wi - wf);
+          if (P.ts && l == 0) stamp_add(P, S, ph, 5, wi - wf);
           tc_fence_after();
           const uint64_t da = sdesc_kmajor_sw128(smem_u32(S.a_tile(stage))) + 2 * l;
           const uint64_t db = sdesc_kmajor_sw128(smem_u32(bb + kb * 2048)) + 2 * l;
@@ -525,7 +625,7 @@ MK_DEV void run_mma(const LayerParams& P, const Smem& S) {
             mma_bf16(d, da, db, idesc_bf16(128, kMaxT), kb != 0);
           }
           mma_commit(&m->empty[stage]);
-          if (P.ts && l == 0) stamp_add(P, ph, 12, globaltimer() - wi);
+          if (P.ts && l == 0) stamp_add(P, S, ph, 12, globaltimer() - wi);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
       }
@@ -536,12 +636,12 @@ MK_DEV void run_mma(const LayerParams& P, const Smem& S) {
       b_ph[b] ^= 1;
       ++ucount;
     }
-    if (l == 0) stamp(P, ph, 2);
+    if (l == 0) stamp(P, S, ph, 2);
   }
   // all issued tensor-core work completes before TMEM is released
   mma_commit(&m->mma_done);
   const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(&m->mma_done, 0)) {
+  while (!mbar_try_wait_sleep(&m->mma_done, 0, 1000u)) {
     if (globaltimer() - t0 > P.timeout_ns) break;
   }
 }
@@ -583,8 +683,9 @@ MK_DEV void issue_bf16(const LayerParams& P, const Smem& S, int ph, const Unit& 
 }
 
 MK_DEV bool stage_bf16(const LayerParams& P, const Smem& S, int ph, const Unit& U, int buf,
-                       uint32_t& land_ph) {
+                       bool issued, uint32_t& land_ph) {
   const int tid = threadIdx.x - kStagerBase;
+  if (!issued && tid == 0) issue_bf16(P, S, ph, U, buf);
   uint8_t* bb = S.bbuf(buf);
   const int nkb = U.nkb;
   const bool gain = bf_source(P, ph).gain != nullptr;
@@ -689,31 +790,31 @@ MK_DEV bool stage_fp4(const LayerParams& P, const Smem& S, const Unit& U, bool g
       __syncwarp();
       if (lane_id() == 0) issue_fp4_row(P, S, U, gu, i, buf, warp);
     }
+    const int s = m->slots[m->off[U.expert] + i];
+    // gate/up rows: the token's scale (phase start); down rows: the scale the
+    // expert's last gate/up tile published, loaded while the row lands
+    const float srow = gu ? m->srow_st[s / P.topk] : __ldcg(P.srow_a + s);
     int wok = 0;
     if (lane_id() == 0) wok = wait_bar(P, S, lb, land_ph[buf][1 + warp], ERR_TIMEOUT_B) ? 1 : 0;
     if (!__shfl_sync(0xffffffffu, wok, 0)) return false;
     land_ph[buf][1 + warp] ^= 1;
     if (lane_id() == 0) m->land_out[buf][1 + warp] = 0;
-    const int s = m->slots[m->off[U.expert] + i];
     OperandSink sink{bb, bb + kBSfOff, static_cast<uint32_t>(i)};
-    quantize_row_given_srow(reinterpret_cast<const __nv_bfloat16*>(slot), K,
-                            gu ? m->srow_st[s / P.topk] : m->srow_st[s], sink);
+    quantize_row_given_srow(reinterpret_cast<const __nv_bfloat16*>(slot), K, srow, sink);
   }
   return true;
 }
 
-// Prefetch of a unit's inputs into operand buffer `buf`'s landing area: the
-// bf16 rows by the stager leader, the first row of each stager warp for
-// NVFP4 units.  Returns whether anything was issued for the NVFP4 case.
+// Prefetch of a unit's inputs into operand buffer `buf`'s landing area, by
+// the stager leader: the bf16 rows, or the first row of each stager warp's
+// slot for NVFP4 units.
 MK_DEV void prefetch_unit(const LayerParams& P, const Smem& S, int ph, const Unit& U, int buf) {
-  const int tid = threadIdx.x - kStagerBase;
   if (!U.fp4) {
-    if (tid == 0) issue_bf16(P, S, ph, U, buf);
+    issue_bf16(P, S, ph, U, buf);
     return;
   }
-  const int w = tid >> 5;
   const int n = S.m->off[U.expert + 1] - S.m->off[U.expert];
-  if (lane_id() == 0 && w < n) issue_fp4_row(P, S, U, ph == PH_GU, w, buf, w);
+  for (int w = 0; w < 2 && w < n; ++w) issue_fp4_row(P, S, U, ph == PH_GU, w, buf, w);
 }
 
 // RMSNorm factors of x_in (first layer), by the stager and epilogue warps: one row per warp at a
@@ -751,14 +852,26 @@ MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
   const int warp = tid >> 5;
   const uint32_t target = grid_target(P, epoch);
   uint32_t b_ph[2] = {0, 0}, ucount = 0, land_ph[2][3] = {{0, 0, 0}, {0, 0, 0}};
+  QCursor q;
   bool ok = true;
   if (P.first_layer) rnorm_x_in(P, S);
   for (int ph = 0; ph < PH_COUNT && ok; ++ph) {
     if (!phase_is_gemm(ph) || !phase_active(P, ph)) continue;
+    if (ph == PH_GU) {
+      // the expert weights depend only on the routing: publish it to the
+      // producer before waiting for the pooler output
+      if (!group_grid_wait(P, S, BAR_ROUTE, target, tid == 0, kBarStage, 64, 0)) { ok = false; break; }
+      if (warp == 0) {
+        build_routing(P, S);
+        __syncwarp();
+        if (lane_id() == 0) mbar_arrive(&m->route_ready);
+      }
+    }
     const int dep = phase_dep(P, ph);
     if (dep >= 0) {
       if (!group_grid_wait(P, S, dep, target, tid == 0, kBarStage, 64, 0)) { ok = false; break; }
     }
+    if (tid == 0) stamp(P, S, ph, 14);
     // per-phase inputs of the token operand
     if (ph == PH_RP || ph == PH_NQKV) {
       const float* ssq = ph == PH_RP ? P.ssq_mid : P.ssq_out;
@@ -768,43 +881,59 @@ MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
         m->rnorm[tid] = 1.0f / sqrtf(s / P.H + P.eps);
       }
     } else if (ph == PH_GU) {
-      if (warp == 0) {
-        build_routing(P, S);
-        __syncwarp();
-        if (lane_id() == 0) mbar_arrive(&m->route_ready);
-      }
       if (tid < P.T) {
         float a = 0.f;
         for (int j = 0; j < P.P / 128; ++j) a = fmaxf(a, __ldcg(P.pamax + j * kMaxT + tid));
         m->srow_st[tid] = a > 0.f ? __fdiv_rn(a, 2688.0f) : 1.0f;
       }
-    } else if (ph == PH_DOWN && P.moe) {
-      for (int s = tid; s < P.T * P.topk; s += 64) {
-        float a = 0.f;
-        for (int j = 0; j < P.I / 128; ++j) a = fmaxf(a, __ldcg(P.aamax + s * (P.I / 128) + j));
-        m->srow_st[s] = a > 0.f ? __fdiv_rn(a, 2688.0f) : 1.0f;
-      }
     }
     stage_sync();
-    const int n = phase_units(P, S, ph);
-    const int u0 = first_unit(P, ph);
-    // the first unit's inputs; every later unit's were issued one unit ahead
-    if (u0 < n) prefetch_unit(P, S, ph, make_unit(P, S, ph, u0), ucount & 1);
-    for (int u = u0; u < n && ok; u += P.grid) {
+    // expert down units wait for their own expert's gate/up tiles, not for
+    // the whole phase: their rows are copied ahead only once it is ready
+    const bool per_expert = ph == PH_DOWN && P.moe;
+    // The leader copies a unit's first inputs ahead into the buffer's landing
+    // area and records whether it did (read by all after the next barrier).
+    auto try_prefetch = [&](const Unit& V, int buf) {
+      if (tid != 0) return;
+      const bool ready = !per_expert ||
+          static_cast<int32_t>(ld_acquire(P.exp_sync + kMaxE + V.expert) - (epoch + 1u)) >= 0;
+      if (ready) prefetch_unit(P, S, ph, V, buf);
+      m->pref_ok[buf] = ready ? 1 : 0;
+    };
+    // the phase's first unit, its inputs copied at once; later units' are
+    // copied one unit ahead when the producer has already claimed them
+    int u;
+    if (!queue_pop_group(P, S, q, u, tid == 0, kBarStage, 64, 0)) { ok = false; break; }
+    if (u >= 0) try_prefetch(make_unit(P, S, ph, u), ucount & 1);
+    while (u >= 0 && ok) {
       const Unit U = make_unit(P, S, ph, u);
       const uint32_t b = ucount & 1;
       // the next unit's inputs go into the other buffer's landing area, which
       // the MMA never reads (its previous contents were consumed last unit)
-      if (u + P.grid < n) prefetch_unit(P, S, ph, make_unit(P, S, ph, u + P.grid), b ^ 1);
+      if (tid == 0) {
+        m->pref_ok[b ^ 1] = 0;
+        if (mbar_test_wait(&m->uq_full[q.slot], q.par)) {
+          const int nu = *reinterpret_cast<volatile int*>(&m->uq[q.slot]);
+          if (nu >= 0) try_prefetch(make_unit(P, S, ph, nu), b ^ 1);
+        }
+      }
       const uint64_t w0 = tnow(P);
       if (!group_mbar_wait(P, S, &m->bempty[b], b_ph[b] ^ 1, ERR_TIMEOUT_B, tid == 0, kBarStage, 64, 0)) {
         ok = false;
         break;
       }
+      const bool pre = *reinterpret_cast<volatile int*>(&m->pref_ok[b]) != 0;
+      if (per_expert && !pre) {
+        // not ready when looked at ahead: wait for the expert now
+        if (!group_flag_wait(P, S, P.exp_sync + kMaxE + U.expert, epoch + 1u, tid == 0, kBarStage, 64, 0)) {
+          ok = false;
+          break;
+        }
+      }
       const uint64_t w1 = tnow(P);
       bool sok = true;
-      if (U.fp4) sok = stage_fp4(P, S, U, ph == PH_GU, b, true, land_ph);
-      else sok = stage_bf16(P, S, ph, U, b, land_ph[b][0]);
+      if (U.fp4) sok = stage_fp4(P, S, U, ph == PH_GU, b, pre, land_ph);
+      else sok = stage_bf16(P, S, ph, U, b, pre, land_ph[b][0]);
       // both stager warps agree on the outcome before the next barrier
       if (lane_id() == 0) m->grp_ok[2 + warp] = sok ? 1 : 0;
       fence_proxy_async_smem();
@@ -816,12 +945,13 @@ MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
       if (tid == 0) {
         mbar_arrive(&m->bfull[b]);
         if (P.ts) {
-          stamp_add(P, ph, 8, w1 - w0);
-          stamp_add(P, ph, 9, globaltimer() - w1);
+          stamp_add(P, S, ph, 8, w1 - w0);
+          stamp_add(P, S, ph, 9, globaltimer() - w1);
         }
       }
       b_ph[b] ^= 1;
       ++ucount;
+      if (!queue_pop_group(P, S, q, u, tid == 0, kBarStage, 64, 0)) { ok = false; break; }
     }
   }
   // landing copies still in flight (only after an abort) must land before exit
@@ -831,7 +961,7 @@ MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
       const int buf = i / 3, sl = i % 3;
       if (!(sl == 0 ? tid == 0 : warp == sl - 1) || !m->land_out[buf][sl]) continue;
       const uint64_t t0 = globaltimer();
-      while (!mbar_try_wait(&m->land[buf][sl], land_ph[buf][sl])) {
+      while (!mbar_try_wait_sleep(&m->land[buf][sl], land_ph[buf][sl], 1000u)) {
         if (globaltimer() - t0 > P.timeout_ns) break;
       }
     }
@@ -866,66 +996,98 @@ MK_DEV float epi_reduce16(const Smem& S, float (&v)[kMaxT], int et, int n) {
   return r;
 }
 
-// Router: top-k of the float32 logits (descending, ties to the lower index),
-// softmax over all experts, combine weights.  One warp per token.
-MK_DEV void router_topk(const LayerParams& P, int et) {
+// Router: top-k of the float32 logits (descending, an exact tie going to the
+// lower expert index), softmax over all experts, combine weights.  Warp w
+// takes tokens w, w+4 together, then w+8, w+12 (their selection steps
+// interleave, hiding each other's latency); lane l holds experts l + 32i as 32-bit
+// order-preserving keys.  A round takes the warp maximum key, then the lowest
+// expert index holding it, and clears that key.
+MK_DEV uint32_t order_key(float v) {
+  const uint32_t b = __float_as_uint(v + 0.0f);  // -0 ranks as +0
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+MK_DEV float key_logit(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+MK_DEV void router_topk_pass(const LayerParams& P, int et, int pass) {
+  constexpr int kQ = 2;           // tokens per warp and pass
+  constexpr int kI = kMaxE / 32;  // experts per lane
   const int w = et >> 5, lane = lane_id();
-  for (int t = w; t < P.T; t += 4) {
-    const float* lg = P.logits + static_cast<size_t>(t) * kMaxE;
-    float v[kMaxE / 32];
-    float mx = -INFINITY;
+  uint32_t key[kQ][kI];
 #pragma unroll
-    for (int i = 0; i < kMaxE / 32; ++i) {
+  for (int q = 0; q < kQ; ++q) {
+    const int t = w + 4 * (2 * pass + q);
+    const float* lg = P.logits + static_cast<size_t>(t < P.T ? t : 0) * kMaxE;
+#pragma unroll
+    for (int i = 0; i < kI; ++i) {
       const int e = lane + 32 * i;
-      v[i] = e < P.E ? __ldcg(lg + e) : -INFINITY;
-      mx = fmaxf(mx, v[i]);
-    }
-    mx = warp_max(mx);
-    float sum = 0.f;
-#pragma unroll
-    for (int i = 0; i < kMaxE / 32; ++i)
-      if (lane + 32 * i < P.E) sum += expf(v[i] - mx);
-    sum = warp_sum(sum);
-    uint32_t taken = 0;
-    float sel_w[kMaxK];
-    int sel_i[kMaxK];
-    for (int r = 0; r < P.topk; ++r) {
-      float best = -INFINITY;
-      int bi = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < kMaxE / 32; ++i) {
-        const int e = lane + 32 * i;
-        if (e < P.E && !((taken >> i) & 1u) && (v[i] > best || (v[i] == best && e < bi))) {
-          best = v[i];
-          bi = e;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      sel_i[r] = bi;
-      sel_w[r] = expf(best - mx) / sum;
-    }
-    if (P.renorm) {
-      float s = 0.f;
-      for (int r = 0; r < P.topk; ++r) s += sel_w[r];
-      for (int r = 0; r < P.topk; ++r) sel_w[r] = sel_w[r] / s;
-    }
-    if (lane < P.topk) {
-      int ii = 0;
-      float ww = 0.f;
-      for (int r = 0; r < P.topk; ++r)
-        if (r == lane) { ii = sel_i[r]; ww = sel_w[r]; }
-      P.idx[t * P.topk + lane] = ii;
-      P.wts[t * P.topk + lane] = ww;
-      if (P.topk_idx_out) P.topk_idx_out[t * P.topk + lane] = ii;
-      if (P.topk_w_out) P.topk_w_out[t * P.topk + lane] = ww;
+      key[q][i] = (t < P.T && e < P.E) ? order_key(__ldcg(lg + e)) : 0u;  // 0: no expert
     }
   }
+  // softmax denominators (max subtracted)
+  float mx[kQ], sum[kQ];
+#pragma unroll
+  for (int q = 0; q < kQ; ++q) {
+    uint32_t m = 0u;
+#pragma unroll
+    for (int i = 0; i < kI; ++i) m = max(m, key[q][i]);
+    mx[q] = key_logit(__reduce_max_sync(0xffffffffu, m));
+    float x = 0.f;
+#pragma unroll
+    for (int i = 0; i < kI; ++i)
+      if (key[q][i] != 0u) x += __expf(key_logit(key[q][i]) - mx[q]);
+    sum[q] = warp_sum(x);
+  }
+  int my_e[kQ];
+  uint32_t my_k[kQ];
+#pragma unroll
+  for (int q = 0; q < kQ; ++q) { my_e[q] = 0; my_k[q] = 0u; }
+  for (int r = 0; r < P.topk; ++r) {
+    uint32_t bk[kQ];
+    int bi[kQ];
+#pragma unroll
+    for (int q = 0; q < kQ; ++q) {
+      bk[q] = 0u;
+      bi[q] = 0;
+#pragma unroll
+      for (int i = kI - 1; i >= 0; --i)
+        if (key[q][i] >= bk[q] && key[q][i] != 0u) { bk[q] = key[q][i]; bi[q] = i; }
+    }
+    uint32_t wk[kQ];
+#pragma unroll
+    for (int q = 0; q < kQ; ++q) wk[q] = __reduce_max_sync(0xffffffffu, bk[q]);
+    int e[kQ];
+#pragma unroll
+    for (int q = 0; q < kQ; ++q)
+      e[q] = static_cast<int>(__reduce_min_sync(
+          0xffffffffu, (bk[q] == wk[q] && wk[q] != 0u) ? static_cast<uint32_t>(bi[q] * 32 + lane) : 0xffffffffu));
+#pragma unroll
+    for (int q = 0; q < kQ; ++q) {
+      if ((e[q] & 31) == lane) {
+#pragma unroll
+        for (int i = 0; i < kI; ++i)
+          if (i == (e[q] >> 5)) key[q][i] = 0u;
+      }
+      if (lane == r) { my_e[q] = e[q]; my_k[q] = wk[q]; }
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < kQ; ++q) {
+    const int t = w + 4 * (2 * pass + q);
+    float wt = lane < P.topk ? __expf(key_logit(my_k[q]) - mx[q]) / sum[q] : 0.f;
+    if (P.renorm) wt = wt / warp_sum(wt);
+    if (t < P.T && lane < P.topk) {
+      P.idx[t * P.topk + lane] = my_e[q];
+      P.wts[t * P.topk + lane] = wt;
+      if (P.topk_idx_out) P.topk_idx_out[t * P.topk + lane] = my_e[q];
+      if (P.topk_w_out) P.topk_w_out[t * P.topk + lane] = wt;
+    }
+  }
+}
+MK_DEV void router_topk(const LayerParams& P, int et) {
+  router_topk_pass(P, et, 0);
+  if (P.T > 8) router_topk_pass(P, et, 1);
 }
 
 // Final values of one 128-row tile of a bf16 phase: acc[j][t] for the row
@@ -1006,7 +1168,7 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
   const uint64_t w0 = tnow(P);
   if (!group_mbar_wait(P, S, &m->accfull[b], acc_ph_b, ERR_TIMEOUT_ACC, et == 0, kBarEpi, 128, 1))
     return false;
-  if (P.ts && et == 0) stamp_add(P, ph, 10, globaltimer() - w0);
+  if (P.ts && et == 0) stamp_add(P, S, ph, 10, globaltimer() - w0);
   acc_ph_b ^= 1;
   tc_fence_after();
   const int q = et >> 5;
@@ -1052,6 +1214,33 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
       }
       const float r = epi_reduce16<true>(S, am, et, n);
       if (et < n) P.aamax[m->slots[m->off[e] + et] * (P.I / 128) + U.tile] = r;
+      // the expert's last finished gate/up tile computes the NVFP4 row scales
+      // of its SwiGLU rows and releases them to the down units
+      epi_sync();
+      if (et == 0) {
+        __threadfence();
+        const uint32_t old = atomicAdd(P.exp_sync + e, 1u);
+        const bool last = old == static_cast<uint32_t>(P.I / 128 - 1);
+        if (last) {
+          P.exp_sync[e] = 0;
+          __threadfence();
+        }
+        m->flag = last;
+      }
+      epi_sync();
+      if (m->flag) {
+        if (et < n) {
+          const int s = m->slots[m->off[e] + et];
+          float a = 0.f;
+          for (int j = 0; j < P.I / 128; ++j) a = fmaxf(a, __ldcg(P.aamax + s * (P.I / 128) + j));
+          P.srow_a[s] = a > 0.f ? __fdiv_rn(a, 2688.0f) : 1.0f;
+        }
+        epi_sync();
+        if (et == 0) {
+          __threadfence();
+          st_release(P.exp_sync + kMaxE + e, m->epoch + 1u);
+        }
+      }
     } else {
       const float td = P.ts_down[e];
       for (int i = 0; i < n; ++i) {
@@ -1137,7 +1326,16 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
     }
     epi_sync();
     if (m->flag) {
+      if (et == 0) stamp(P, S, PH_COUNT, 3);
       router_topk(P, et);
+      if (et == 0) stamp(P, S, PH_COUNT, 6);
+      epi_sync();
+      if (et == 0) stamp(P, S, PH_COUNT, 7);
+      if (et == 0) {
+        __threadfence();
+        red_release_add(P.bar_ctr + BAR_ROUTE, static_cast<uint32_t>(P.grid));
+        stamp(P, S, PH_COUNT, 4);
+      }
     }
   }
   return true;
@@ -1454,13 +1652,14 @@ MK_DEV void run_epilogue(const LayerParams& P, const Smem& S, uint32_t epoch) {
   const int et = threadIdx.x - kEpiBase;  // 0..127
   const uint32_t target = grid_target(P, epoch);
   uint32_t acc_ph[2] = {0, 0}, ucount = 0;
+  QCursor qe;
   bool ok = true;
   if (P.first_layer) rnorm_x_in(P, S);
   const int last_ph = P.fuse_next ? PH_NQKV : (P.moe ? PH_UNPOOL : PH_DOWN);
   for (int ph = 0; ph < PH_COUNT && ok; ++ph) {
     if (!phase_active(P, ph)) continue;
     if (ph == last_ph && et == 0) pdl_launch_dependents();
-    if (et == 0) stamp(P, ph, 0);
+    if (et == 0) stamp(P, S, ph, 0);
     if (ph == PH_ATTN) {
       if (P.first_layer && !(ok = epi_wait(P, S, BAR_QKV, target, et))) break;
       const int n = phase_units(P, S, ph);
@@ -1471,7 +1670,7 @@ MK_DEV void run_epilogue(const LayerParams& P, const Smem& S, uint32_t epoch) {
         if (P.d == 128) attention_unit<128>(P, S, g, lo, hi, c, et);
         else attention_unit<64>(P, S, g, lo, hi, c, et);
       }
-      if (et == 0) stamp(P, ph, 1);
+      if (et == 0) stamp(P, S, ph, 1);
       epi_arrive(P, S, BAR_ATTN, et);
       continue;
     }
@@ -1485,7 +1684,7 @@ MK_DEV void run_epilogue(const LayerParams& P, const Smem& S, uint32_t epoch) {
         if (P.d == 128) merge_item<128>(P, u);
         else merge_item<64>(P, u);
       }
-      if (et == 0) stamp(P, ph, 1);
+      if (et == 0) stamp(P, S, ph, 1);
       epi_arrive(P, S, BAR_MERGE, et);
       continue;
     }
@@ -1501,32 +1700,42 @@ MK_DEV void run_epilogue(const LayerParams& P, const Smem& S, uint32_t epoch) {
       }
       epi_sync();
     } else if (ph == PH_DOWN && P.moe) {
-      if (!(ok = epi_wait(P, S, BAR_GU, target, et))) break;
       for (int i = et; i < kMaxT * 16; i += 128) (&m->comb_local[0][0])[i] = 0;
-      for (int s = et; s < P.T * P.topk; s += 128) {
-        float a = 0.f;
-        for (int j = 0; j < P.I / 128; ++j) a = fmaxf(a, __ldcg(P.aamax + s * (P.I / 128) + j));
-        m->srow_ep[s] = a > 0.f ? __fdiv_rn(a, 2688.0f) : 1.0f;
-      }
       epi_sync();
     }
-    const int n = phase_units(P, S, ph);
-    for (int u = first_unit(P, ph); u < n && ok; u += P.grid) {
+    if (et == 0) stamp(P, S, ph, 15);
+    while (ok) {
+      int u;
+      if (!queue_pop_group(P, S, qe, u, et == 0, kBarEpi, 128, 1)) { ok = false; break; }
+      if (u < 0) break;
       const Unit U = make_unit(P, S, ph, u);
       const uint32_t b = ucount & 1;
       const uint64_t w0 = tnow(P);
+      if (ph == PH_DOWN && P.moe) {
+        if (!(ok = group_flag_wait(P, S, P.exp_sync + kMaxE + U.expert, epoch + 1u, et == 0, kBarEpi, 128, 1)))
+          break;
+        const int e = U.expert;
+        if (et < m->off[e + 1] - m->off[e]) {
+          const int s = m->slots[m->off[e] + et];
+          m->srow_ep[s] = __ldcg(P.srow_a + s);
+        }
+        epi_sync();
+      }
       ok = epi_gemm_unit(P, S, ph, U, b, acc_ph[b], et);
-      if (P.ts && et == 0) stamp_add(P, ph, 11, globaltimer() - w0);
+      if (P.ts && et == 0) stamp_add(P, S, ph, 11, globaltimer() - w0);
       ++ucount;
     }
     if (!ok) break;
     if (ph == PH_DOWN && P.moe) combine_phase_end(P, S, et);
-    if (et == 0) stamp(P, ph, 1);
+    if (et == 0) stamp(P, S, ph, 1);
     epi_arrive(P, S, phase_arrive(P, ph), et);
   }
   // CTA 0 advances the epoch once every CTA has finished this launch.
   if (ok && blockIdx.x == 0) {
     if (epi_wait(P, S, final_barrier(P), target, et) && et == 0) {
+      // every CTA has claimed its last unit: the counters start the next
+      // launch at zero
+      for (int i = 0; i < PH_COUNT; ++i) P.sched[i] = 0;
       __threadfence();
       *P.epoch = epoch + 1u;
     }
@@ -1540,9 +1749,12 @@ __global__ void __launch_bounds__(kThreads, 1) mk_layer_kernel(const __grid_cons
   S.base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                       ~static_cast<uintptr_t>(1023));
   S.m = reinterpret_cast<Misc*>(S.base + kOffMisc);
+  S.ts = reinterpret_cast<uint64_t*>(S.base + kOffTs);
   const int warp = threadIdx.x >> 5;
   Misc* m = S.m;
-  if (threadIdx.x == 0) stamp(P, PH_COUNT, 0);
+  const uint64_t t_start = P.ts ? globaltimer() : 0;
+  if (P.ts)
+    for (int i = threadIdx.x; i < kTsPerCta; i += kThreads) S.ts[i] = 0;
 
   if (threadIdx.x == 0) {
     // barriers completed by tcgen05.commit count the four MMA lanes
@@ -1558,6 +1770,10 @@ __global__ void __launch_bounds__(kThreads, 1) mk_layer_kernel(const __grid_cons
     }
     mbar_init(&m->route_ready, 1);
     mbar_init(&m->mma_done, 4);
+    for (int i = 0; i < kUQ; ++i) {
+      mbar_init(&m->uq_full[i], 1);
+      mbar_init(&m->uq_empty[i], 6);  // 4 MMA issuers, stager and epilogue leaders
+    }
     for (int i = 0; i < 6; ++i) mbar_init(&m->land[i / 3][i % 3], 1);
     m->abort = 0;
     m->n_act = 0;
@@ -1571,6 +1787,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_layer_kernel(const __grid_cons
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (P.ts && threadIdx.x == 0) S.ts[PH_COUNT * kTsSlots] = t_start;
 
   if (warp == 0) {
     // weights depend on nothing in flight: stream them before the previous
@@ -1582,7 +1799,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_layer_kernel(const __grid_cons
     // advances the epoch only after every CTA has arrived on the last counter.
     if (threadIdx.x == 32) m->epoch = *reinterpret_cast<volatile uint32_t*>(P.epoch);
     named_bar(3, kThreads - 32);
-    if (threadIdx.x == 32) stamp(P, PH_COUNT, 1);
+    if (threadIdx.x == 32) stamp(P, S, PH_COUNT, 1);
     const uint32_t epoch = m->epoch;
     if (warp >= 1 && warp <= 4) {
       if (lane_id() == 0) run_mma(P, S);
@@ -1598,7 +1815,12 @@ __global__ void __launch_bounds__(kThreads, 1) mk_layer_kernel(const __grid_cons
     tc_fence_after();
     tmem_dealloc(m->tmem_base, kTmemCols);
   }
-  if (threadIdx.x == 0) stamp(P, PH_COUNT, 2);
+  if (P.ts) {
+    if (threadIdx.x == 0) stamp(P, S, PH_COUNT, 2);
+    __syncthreads();
+    for (int i = threadIdx.x; i < kTsPerCta; i += kThreads)
+      P.ts[static_cast<size_t>(blockIdx.x) * kTsPerCta + i] = S.ts[i];
+  }
 }
 
 const void* layer_kernel_ptr() { return reinterpret_cast<const void*>(&mk_layer_kernel); }

@@ -42,7 +42,8 @@ enum BarrierId : int {
   BAR_GU = 5,     // expert SwiGLU rows and their amax partials written
   BAR_DOWN = 6,   // z slots and the combined y written
   BAR_X = 7,      // x_out and its sum-of-squares partials written
-  BAR_END = 8     // next layer's q and K/V rows written
+  BAR_END = 8,    // next layer's q and K/V rows written
+  BAR_ROUTE = 9   // router top-k written (one CTA adds grid)
 };
 
 struct LayerParams {
@@ -108,18 +109,26 @@ struct LayerParams {
   float* attn_part;         // [Hkv*chunks][64][d + 2]
   uint32_t* fix_ctr;        // fixup counters per (phase, tile)  [PH_COUNT][256]
   uint32_t* comb_ctr;       // combine counters [16][P/128]
+  uint32_t* exp_sync;       // MoE: [0, 256) finished gate/up tiles per expert (the
+                            // last one resets it), [256, 512) expert's SwiGLU rows
+                            // and their scales ready (epoch + 1)
+  float* srow_a;            // MoE: NVFP4 row scales of the SwiGLU rows [16*k]
   uint32_t* misc_ctr;       // [0]: router tiles done
+  uint32_t* sched;          // [PH_COUNT] next unclaimed unit of each phase (reset by CTA 0 at the end)
   uint32_t* bar_ctr;        // [kNumCounters] grid dependency counters
   uint32_t* epoch;          // launches of this layer so far
   uint32_t* status;         // sticky error word
-  // self-timing (optional, nullptr when off): %globaltimer stamps per CTA,
+  // self-timing (optional, nullptr when off): %globaltimer stamps per CTA of
+  // the last launch (kept in shared memory, written out at CTA exit),
   // [grid][PH_COUNT + 1][kTsSlots]: per phase 0 epilogue start, 1 epilogue
   // end, 2 last MMA issued, 3 last weight tile issued, then nanoseconds spent
   // 4 producer waiting for a free stage, 5 MMA waiting for weights, 6 MMA
   // waiting for the token operand, 7 MMA waiting for a free accumulator,
   // 8 stager waiting for a free operand buffer, 9 stager working, 10 epilogue
-  // waiting for an accumulator, 11 epilogue working; last row: kernel start,
-  // inputs ready, kernel end; 12 MMA issuing (weights ready to commit).
+  // waiting for an accumulator, 11 epilogue working; 12 MMA issuing (weights
+  // ready to commit); 13 MMA starts the phase's units, 14 stagers' input
+  // dependency met, 15 epilogue starts the phase's units.  Last row: kernel
+  // start, inputs ready, kernel end, router top-k start and release.
   uint64_t* ts;
 };
 constexpr int kTsSlots = 16;
