@@ -1010,84 +1010,75 @@ MK_DEV float key_logit(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-MK_DEV void router_topk_pass(const LayerParams& P, int et, int pass) {
-  constexpr int kQ = 2;           // tokens per warp and pass
+// The code runs once per launch on one SM, so its cost is mostly fetching its
+// instructions: loops, not unrolled copies, except over a lane's 8 experts.
+MK_DEV void router_topk(const LayerParams& P, int et) {
   constexpr int kI = kMaxE / 32;  // experts per lane
   const int w = et >> 5, lane = lane_id();
-  uint32_t key[kQ][kI];
-#pragma unroll
-  for (int q = 0; q < kQ; ++q) {
-    const int t = w + 4 * (2 * pass + q);
-    const float* lg = P.logits + static_cast<size_t>(t < P.T ? t : 0) * kMaxE;
+#pragma unroll 1
+  for (int pass = 0; pass < 2; ++pass) {
+    const int t0 = w + 8 * pass, t1 = t0 + 4;  // two tokens per pass
+    if (t0 >= P.T) break;
+    uint32_t k0[kI], k1[kI];
+    const float* l0 = P.logits + static_cast<size_t>(t0) * kMaxE;
+    const float* l1 = P.logits + static_cast<size_t>(t1 < P.T ? t1 : t0) * kMaxE;
 #pragma unroll
     for (int i = 0; i < kI; ++i) {
       const int e = lane + 32 * i;
-      key[q][i] = (t < P.T && e < P.E) ? order_key(__ldcg(lg + e)) : 0u;  // 0: no expert
+      k0[i] = e < P.E ? order_key(__ldcg(l0 + e)) : 0u;  // 0: no expert
+      k1[i] = (e < P.E && t1 < P.T) ? order_key(__ldcg(l1 + e)) : 0u;
     }
-  }
-  // softmax denominators (max subtracted)
-  float mx[kQ], sum[kQ];
+    // softmax denominators (max subtracted)
+    uint32_t m0 = 0u, m1 = 0u;
 #pragma unroll
-  for (int q = 0; q < kQ; ++q) {
-    uint32_t m = 0u;
+    for (int i = 0; i < kI; ++i) { m0 = max(m0, k0[i]); m1 = max(m1, k1[i]); }
+    const float mx0 = key_logit(__reduce_max_sync(0xffffffffu, m0));
+    const float mx1 = key_logit(__reduce_max_sync(0xffffffffu, m1));
+    float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-    for (int i = 0; i < kI; ++i) m = max(m, key[q][i]);
-    mx[q] = key_logit(__reduce_max_sync(0xffffffffu, m));
-    float x = 0.f;
-#pragma unroll
-    for (int i = 0; i < kI; ++i)
-      if (key[q][i] != 0u) x += __expf(key_logit(key[q][i]) - mx[q]);
-    sum[q] = warp_sum(x);
-  }
-  int my_e[kQ];
-  uint32_t my_k[kQ];
-#pragma unroll
-  for (int q = 0; q < kQ; ++q) { my_e[q] = 0; my_k[q] = 0u; }
-  for (int r = 0; r < P.topk; ++r) {
-    uint32_t bk[kQ];
-    int bi[kQ];
-#pragma unroll
-    for (int q = 0; q < kQ; ++q) {
-      bk[q] = 0u;
-      bi[q] = 0;
-#pragma unroll
-      for (int i = kI - 1; i >= 0; --i)
-        if (key[q][i] >= bk[q] && key[q][i] != 0u) { bk[q] = key[q][i]; bi[q] = i; }
+    for (int i = 0; i < kI; ++i) {
+      if (k0[i] != 0u) s0 += __expf(key_logit(k0[i]) - mx0);
+      if (k1[i] != 0u) s1 += __expf(key_logit(k1[i]) - mx1);
     }
-    uint32_t wk[kQ];
+    s0 = warp_sum(s0);
+    s1 = warp_sum(s1);
+    int e0 = 0, e1 = 0;
+    uint32_t w0 = 0u, w1 = 0u;
+#pragma unroll 1
+    for (int r = 0; r < P.topk; ++r) {
+      uint32_t b0 = 0u, b1 = 0u;
+      int i0 = 0, i1 = 0;
 #pragma unroll
-    for (int q = 0; q < kQ; ++q) wk[q] = __reduce_max_sync(0xffffffffu, bk[q]);
-    int e[kQ];
-#pragma unroll
-    for (int q = 0; q < kQ; ++q)
-      e[q] = static_cast<int>(__reduce_min_sync(
-          0xffffffffu, (bk[q] == wk[q] && wk[q] != 0u) ? static_cast<uint32_t>(bi[q] * 32 + lane) : 0xffffffffu));
-#pragma unroll
-    for (int q = 0; q < kQ; ++q) {
-      if ((e[q] & 31) == lane) {
-#pragma unroll
-        for (int i = 0; i < kI; ++i)
-          if (i == (e[q] >> 5)) key[q][i] = 0u;
+      for (int i = kI - 1; i >= 0; --i) {
+        if (k0[i] >= b0 && k0[i] != 0u) { b0 = k0[i]; i0 = i; }
+        if (k1[i] >= b1 && k1[i] != 0u) { b1 = k1[i]; i1 = i; }
       }
-      if (lane == r) { my_e[q] = e[q]; my_k[q] = wk[q]; }
-    }
-  }
+      const uint32_t x0 = __reduce_max_sync(0xffffffffu, b0), x1 = __reduce_max_sync(0xffffffffu, b1);
+      const int c0 = static_cast<int>(__reduce_min_sync(
+          0xffffffffu, (b0 == x0 && x0 != 0u) ? static_cast<uint32_t>(i0 * 32 + lane) : 0xffffffffu));
+      const int c1 = static_cast<int>(__reduce_min_sync(
+          0xffffffffu, (b1 == x1 && x1 != 0u) ? static_cast<uint32_t>(i1 * 32 + lane) : 0xffffffffu));
 #pragma unroll
-  for (int q = 0; q < kQ; ++q) {
-    const int t = w + 4 * (2 * pass + q);
-    float wt = lane < P.topk ? __expf(key_logit(my_k[q]) - mx[q]) / sum[q] : 0.f;
-    if (P.renorm) wt = wt / warp_sum(wt);
-    if (t < P.T && lane < P.topk) {
-      P.idx[t * P.topk + lane] = my_e[q];
-      P.wts[t * P.topk + lane] = wt;
-      if (P.topk_idx_out) P.topk_idx_out[t * P.topk + lane] = my_e[q];
-      if (P.topk_w_out) P.topk_w_out[t * P.topk + lane] = wt;
+      for (int i = 0; i < kI; ++i) {
+        if ((c0 & 31) == lane && i == (c0 >> 5)) k0[i] = 0u;
+        if ((c1 & 31) == lane && i == (c1 >> 5)) k1[i] = 0u;
+      }
+      if (lane == r) { e0 = c0; w0 = x0; e1 = c1; w1 = x1; }
+    }
+#pragma unroll 1
+    for (int q = 0; q < 2; ++q) {
+      const int t = q ? t1 : t0;
+      const int e = q ? e1 : e0;
+      float wt = lane < P.topk ? __expf(key_logit(q ? w1 : w0) - (q ? mx1 : mx0)) / (q ? s1 : s0) : 0.f;
+      if (P.renorm) wt = wt / warp_sum(wt);
+      if (t < P.T && lane < P.topk) {
+        P.idx[t * P.topk + lane] = e;
+        P.wts[t * P.topk + lane] = wt;
+        if (P.topk_idx_out) P.topk_idx_out[t * P.topk + lane] = e;
+        if (P.topk_w_out) P.topk_w_out[t * P.topk + lane] = wt;
+      }
     }
   }
-}
-MK_DEV void router_topk(const LayerParams& P, int et) {
-  router_topk_pass(P, et, 0);
-  if (P.T > 8) router_topk_pass(P, et, 1);
 }
 
 // Final values of one 128-row tile of a bf16 phase: acc[j][t] for the row
