@@ -95,6 +95,45 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 
+# ------------------------------------------------------------------ replicas
+def replica_seed(workload, rank):
+    """Seed of rank `rank`'s inputs: replicas run independent problems."""
+    from moe_decode_layer_persistent_gb300 import synth
+    return synth.SEED_BASE + synth.WORKLOADS[workload]["index"] + 1000 * rank
+
+
+def max_over_ranks(x, device):
+    """The slowest rank's time (every rank gets it)."""
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ ncu traffic
+def kernel_source_hash():
+    import glob
+    import hashlib
+    files = sorted(glob.glob(os.path.join(ROOT, "moe_decode_layer_persistent_gb300", "csrc", "*")))
+    return hashlib.sha256(b"".join(open(f, "rb").read() for f in files)).hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes (read + write) per launch from the committed ncu summary of
+    this workload, or None when there is none or the kernel sources changed
+    since it was captured."""
+    path = os.path.join(ROOT, "profiles", "mk_layer_kernel_%s.md" % workload)
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    for ln in open(path):
+        if ":" in ln:
+            k, v = ln.split(":", 1)
+            fields[k.strip()] = v.strip()
+    if fields.get("source_hash") != kernel_source_hash() or "traffic_bytes_per_launch" not in fields:
+        return None
+    return int(fields["traffic_bytes_per_launch"])
+
+
 # ------------------------------------------------------------------ workloads
 def algorithmic_bytes(c, T, ctx, n_experts_touched, first, fuse):
     """Bytes one layer launch must move at least (weights read once, KV read
@@ -256,8 +295,7 @@ def main():
     torch.cuda.set_device(local_rank)
     from moe_decode_layer_persistent_gb300 import binding as B
     # each replica draws its own inputs (seed offset by rank)
-    work = synth.make_workload(args.workload, device="cuda",
-                               seed=synth.SEED_BASE + synth.WORKLOADS[args.workload]["index"] + 1000 * rank)
+    work = synth.make_workload(args.workload, device="cuda", seed=replica_seed(args.workload, rank))
     stream = torch.cuda.Stream()
     R = Runner(B, work, stream)
     wl = work["wl"]
@@ -304,24 +342,26 @@ def main():
     if st != 0:
         raise RuntimeError("device status %s in timed region" % B.mk_status_string(st))
     if world > 1:
-        t = torch.tensor([ms_step], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
+        ms_step = max_over_ranks(ms_step, "cuda")
 
-    # e2e: host buffers, pinned H2D of x_in and D2H of x_out in every step
+    # e2e: host buffers, pinned H2D of x_in and D2H of x_out inside every
+    # step's events; the L2 flush (single-layer workloads) stays outside them
     x_host = work["x_in"].cpu().pin_memory()
     y_host = torch.empty_like(x_host).pin_memory()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    evs2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(args.steps)]
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
-        e0.record(stream)
         for i in range(args.steps):
+            if flush is not None:
+                flush.fill_(float(i))
+            evs2[i][0].record(stream)
             R.x_in.copy_(x_host, non_blocking=True)
             R.step()
             y_host.copy_(R.x_out, non_blocking=True)
-        e1.record(stream)
+            evs2[i][1].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
+    e2e_ms = sum(a.elapsed_time(b) for a, b in evs2) / args.steps
     bytes_io = x_host.numel() * x_host.element_size()
 
     # roofline of the layer kernel (the only kernel of the step)
@@ -351,7 +391,8 @@ def main():
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "frac_of_8TBs": round(achieved / 8000.0, 4),
-                     "algorithmic_bytes_per_launch": int(alg_per_launch), "traffic": None},
+                     "algorithmic_bytes_per_launch": int(alg_per_launch),
+                     "traffic": profiled_traffic(args.workload)},
         "e2e": {"value": round(e2e_ms * 1e3, 3), "unit": "us/step",
                 "h2d_bytes_per_step": bytes_io, "d2h_bytes_per_step": bytes_io},
         "gpu_launches": args.steps * R.launches_per_step,
