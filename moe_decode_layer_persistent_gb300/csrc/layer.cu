@@ -503,6 +503,13 @@ MK_DEV void build_routing(const LayerParams& P, const Smem& S) {
 // ============================================================ producer (warp 0)
 MK_DEV int first_gemm_phase(const LayerParams& P) { return P.first_layer ? PH_QKV : PH_O; }
 
+// L2 prefetch of this CTA's 1/grid share of a bf16 weight matrix [N][K]
+// (128-row x 64-column tiles of its tensor map).
+MK_DEV void prefetch_share_l2(const LayerParams& P, const CUtensorMap* map, int N, int K) {
+  const int kt = K / 64, nt = (N + 127) / 128;
+  for (int i = blockIdx.x; i < nt * kt; i += P.grid) tma_prefetch_2d(map, (i % kt) * 64, (i / kt) * 128);
+}
+
 MK_DEV void run_producer(const LayerParams& P, const Smem& S) {
   Misc* m = S.m;
   const uint64_t pol = policy_evict_first();
@@ -514,25 +521,34 @@ MK_DEV void run_producer(const LayerParams& P, const Smem& S) {
   for (int ph = 0; ph < PH_COUNT && ok; ++ph) {
     if (!phase_is_gemm(ph) || !phase_active(P, ph)) continue;
     if (P.moe && ph == PH_GU && !route_known) {
+      // HBM idles while the router picks the experts: fetch this CTA's share
+      // of the weights that do not depend on the routing (unpooler, fused
+      // next-layer QKV) into L2 meanwhile
+      prefetch_share_l2(P, &P.tm_unpool, P.H, P.P);
+      if (P.fuse_next) prefetch_share_l2(P, &P.tm_nqkv, P.Nqkv, P.H);
       if (!wait_bar(P, S, &m->route_ready, 0, ERR_TIMEOUT_ROUTE)) { ok = false; break; }
       route_known = true;
     }
-    // claimed units: the previous launch of this layer (which resets the
-    // counters at its end) must be complete
-    const bool claimed = ph != ph0;
-    if (claimed && !prev_done) {
-      pdl_wait();
-      prev_done = true;
-    }
+    // The launch's first weight phase starts with one unit per CTA dealt
+    // statically (streamed before the previous launch ends); all other units
+    // are claimed from the phase's counter, once the previous launch of this
+    // layer (which resets the counters at its end) is complete.
     const int n = phase_units(P, S, ph);
+    bool first = ph == ph0;
     int u = first_unit(P, ph);
     while (ok) {
-      if (claimed) u = static_cast<int>(atomicAdd(P.sched + ph, 1u));
+      if (!first) {
+        if (!prev_done) {
+          pdl_wait();
+          prev_done = true;
+        }
+        u = static_cast<int>(atomicAdd(P.sched + ph, 1u)) + (ph == ph0 ? P.grid : 0);
+      }
+      first = false;
       const bool end = u >= n;
       if (!queue_push(P, S, q, end ? -1 : u)) { ok = false; break; }
       if (end) break;
       const Unit U = make_unit(P, S, ph, u);
-      if (!claimed) u += P.grid;
       const uint32_t bytes = kTileBytes + (U.fp4 ? kSfBytes : 0);
       for (int kb = 0; kb < U.nkb && ok; ++kb) {
         for (int j = 0; j < U.pair; ++j) {
