@@ -109,6 +109,16 @@ def max_over_ranks(x, device):
     return float(t.item())
 
 
+def expert_prefetch_line(a, b):
+    """Expert-prefetch statistics of the timed steps: hit_rate = share of the
+    active experts that were prefetched, precision = share of the prefetched
+    experts that were active."""
+    d = {k: b[k] - a[k] for k in b}
+    return {"predicted_per_step": round(d["predicted"] / max(d["steps"], 1), 2),
+            "hit_rate": round(d["hits"] / d["active"], 4) if d["active"] else None,
+            "precision": round(d["hits"] / d["predicted"], 4) if d["predicted"] else None}
+
+
 # ------------------------------------------------------------------ ncu traffic
 def kernel_source_hash():
     import glob
@@ -160,7 +170,7 @@ def algorithmic_bytes(c, T, ctx, n_experts_touched, first, fuse):
     return b
 
 
-def build_layers(B, work):
+def build_layers(B, work, prefetch_experts=None):
     cfgs, Ws = work["cfgs"], work["Ws"]
     L = len(Ws)
     max_ctx = work["caches"][0][0].shape[0]
@@ -168,7 +178,7 @@ def build_layers(B, work):
     for l in range(L):
         fuse = l + 1 < L or (L == 1 and work["next"] is not None)
         flags = (B.MK_FIRST_LAYER if l == 0 else 0) | (B.MK_FUSE_NEXT_QKV if fuse else 0)
-        cfg = B.make_config(cfgs[l], flags=flags, max_ctx=max_ctx)
+        cfg = B.make_config(cfgs[l], flags=flags, max_ctx=max_ctx, prefetch_experts=prefetch_experts)
         wd = dict(Ws[l])
         nxt = Ws[l + 1] if l + 1 < L else work["next"]
         if fuse:
@@ -180,11 +190,11 @@ def build_layers(B, work):
 class Runner:
     """Holds the device state of one replica and runs steps."""
 
-    def __init__(self, B, work, stream):
+    def __init__(self, B, work, stream, prefetch_experts=None):
         self.B, self.work, self.stream = B, work, stream
         wl = work["wl"]
         self.T, self.ctx = wl["T"], wl["ctx"]
-        self.layers = build_layers(B, work)
+        self.layers = build_layers(B, work, prefetch_experts)
         self.L = len(self.layers)
         self.stack = B.mk_stack_create(self.layers) if self.L > 1 else None
         self.kcs = [c[0] for c in work["caches"]]
@@ -220,11 +230,27 @@ class Runner:
         return self.B.mk_stack_status(self.stack) if self.stack is not None else \
             self.B.mk_layer_status(self.layers[0])
 
-    def experts_touched(self):
+    def drift(self, gen):
+        """Next step's input of a MoE workload: x <- 0.9 x + sqrt(0.19) n,
+        n ~ N(0, 1), so that consecutive steps route partly alike (the
+        previous step's most-used experts are the prefetch's prediction)."""
+        if not self.moe:
+            return
+        n = torch.randn(self.x_in.shape, generator=gen, device="cuda", dtype=torch.float32)
+        self.x_in.copy_((0.9 * self.x_in.float() + 0.19 ** 0.5 * n).to(torch.bfloat16))
+
+    def experts_touched(self, hist=None):
+        """Distinct experts per layer, averaged over the recorded steps."""
         if not self.moe:
             return [0] * self.L
-        idx = self.idx.cpu().numpy()
-        return [len(set(idx[l].ravel().tolist())) for l in range(self.L)]
+        h = (self.idx[None] if hist is None else hist).cpu().numpy()
+        return [float(np.mean([len(set(h[i, l].ravel().tolist())) for i in range(h.shape[0])]))
+                for l in range(self.L)]
+
+    def prefetch_stats(self):
+        if self.stack is not None:
+            return self.B.mk_stack_prefetch_stats(self.stack)
+        return self.B.mk_layer_prefetch_stats(self.layers[0])
 
     def close(self):
         if self.stack is not None:
@@ -279,6 +305,9 @@ def main():
     ap.add_argument("--workload", default="swa_layer")
     ap.add_argument("--impl", default="mk", choices=["mk", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefetch-experts", type=int, default=None,
+                    help="MoE: experts of the previous step prefetched into L2 (default 0: "
+                         "off, measured faster on these inputs)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -297,13 +326,17 @@ def main():
     # each replica draws its own inputs (seed offset by rank)
     work = synth.make_workload(args.workload, device="cuda", seed=replica_seed(args.workload, rank))
     stream = torch.cuda.Stream()
-    R = Runner(B, work, stream)
+    R = Runner(B, work, stream, prefetch_experts=args.prefetch_experts)
     wl = work["wl"]
     single = R.L == 1
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda") if single else None
 
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(replica_seed(args.workload, rank) + 7)
+    hist = torch.zeros((args.steps,) + tuple(R.idx.shape), dtype=torch.int32, device="cuda")
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
+            R.drift(gen)
             if flush is not None:
                 flush.fill_(1.0)
             R.step()
@@ -322,15 +355,19 @@ def main():
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    pf0 = R.prefetch_stats() if R.moe else None
     t_wall0 = time.perf_counter()
     with torch.cuda.stream(stream):
         for i in range(args.steps):
+            R.drift(gen)
             if flush is not None:
                 flush.fill_(float(i))
             evs[i][0].record(stream)
             R.step()
             evs[i][1].record(stream)
+            hist[i].copy_(R.idx)
     torch.cuda.synchronize()
+    pf1 = R.prefetch_stats() if R.moe else None
     t_wall = time.perf_counter() - t_wall0
     if world > 1:
         torch.distributed.barrier()
@@ -365,7 +402,7 @@ def main():
     bytes_io = x_host.numel() * x_host.element_size()
 
     # roofline of the layer kernel (the only kernel of the step)
-    touched = R.experts_touched()
+    touched = R.experts_touched(hist)
     first_flags = [l == 0 for l in range(R.L)]
     fuse_flags = [(l + 1 < R.L) or (R.L == 1 and work["next"] is not None) for l in range(R.L)]
     alg = [algorithmic_bytes(work["cfgs"][l], R.T, R.ctx, touched[l], first_flags[l], fuse_flags[l])
@@ -388,6 +425,9 @@ def main():
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "us_per_layer": round(us_step / R.L, 3),
         "experts_touched_mean": round(float(np.mean(touched)), 2) if R.moe else None,
+        "inputs": ("x_{s+1} = 0.9 x_s + 0.436 n_s per step (consecutive steps route partly alike)"
+                   if R.moe else "the same x_in every step"),
+        "expert_prefetch": expert_prefetch_line(pf0, pf1) if R.moe else None,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "frac_of_8TBs": round(achieved / 8000.0, 4),

@@ -84,6 +84,12 @@ typedef struct mk_layer_config {
   int32_t max_ctx;        /* KV capacity in positions (rows of each cache)       */
   float rms_eps;          /* RMSNorm epsilon; 0 selects 1e-6                      */
   uint32_t flags;         /* MK_FIRST_LAYER | MK_FUSE_NEXT_QKV | MK_TOPK_RENORM  */
+  int32_t prefetch_experts; /* MoE, 0..16: while the router picks this step's
+                               experts, the weights of the previous step's N
+                               most-used experts are fetched into L2 (page
+                               "Muse Spark Open: 1,109 Tokens a Second ...",
+                               section "Three bills a kernel this big has to
+                               pay": the 14 most-used experts); 0 = off       */
   uint64_t wait_timeout_ns; /* bound on every device-side wait; 0 -> 200 ms      */
 } mk_layer_config;
 
@@ -184,6 +190,21 @@ typedef struct mk_stack_io {
 mk_status mk_stack_step(mk_stack* stack, const mk_stack_io* io, void* stream);
 mk_status mk_stack_status(mk_stack* stack);
 void mk_stack_destroy(mk_stack* stack);
+
+/* Expert-prefetch statistics of a layer (MoE, prefetch_experts > 0), summed
+ * over its steps since creation: `predicted` experts prefetched, `active`
+ * experts the steps routed to, `hits` prefetched experts that were active.
+ * hits / active is the share of expert weights that the prefetch covered.
+ * Reads device counters synchronously: call after synchronising. */
+typedef struct mk_prefetch_stats {
+  uint64_t steps;
+  uint64_t predicted;
+  uint64_t active;
+  uint64_t hits;
+} mk_prefetch_stats;
+mk_status mk_layer_prefetch_stats(mk_layer* layer, mk_prefetch_stats* out);
+/* The same summed over the stack's layers. */
+mk_status mk_stack_prefetch_stats(mk_stack* stack, mk_prefetch_stats* out);
 
 /* Human-readable name of a status code (static storage). */
 const char* mk_status_string(mk_status s);

@@ -42,7 +42,13 @@ class mk_layer_config(ctypes.Structure):
                 ("pooled_dim", ctypes.c_int32), ("expert_inter", ctypes.c_int32),
                 ("dense_inter", ctypes.c_int32), ("max_tokens", ctypes.c_int32),
                 ("max_ctx", ctypes.c_int32), ("rms_eps", ctypes.c_float),
-                ("flags", ctypes.c_uint32), ("wait_timeout_ns", ctypes.c_uint64)]
+                ("flags", ctypes.c_uint32), ("prefetch_experts", ctypes.c_int32),
+                ("wait_timeout_ns", ctypes.c_uint64)]
+
+
+class mk_prefetch_stats(ctypes.Structure):
+    _fields_ = [("steps", ctypes.c_uint64), ("predicted", ctypes.c_uint64),
+                ("active", ctypes.c_uint64), ("hits", ctypes.c_uint64)]
 
 
 _WEIGHT_FIELDS = ["attn_norm_w", "w_qkv", "w_o", "ffn_norm_w", "w_router", "w_pool", "w_unpool",
@@ -92,6 +98,8 @@ _lib_mk_layer_destroy = _sig("mk_layer_destroy", None, [_vp])
 _lib_mk_stack_create = _sig("mk_stack_create", _c.c_int, [_c.POINTER(_vp), _c.c_int32, _c.POINTER(_vp)])
 _lib_mk_stack_step = _sig("mk_stack_step", _c.c_int, [_vp, _c.POINTER(mk_stack_io), _vp])
 _lib_mk_stack_status = _sig("mk_stack_status", _c.c_int, [_vp])
+_lib_mk_layer_prefetch_stats = _sig("mk_layer_prefetch_stats", _c.c_int, [_vp, _vp])
+_lib_mk_stack_prefetch_stats = _sig("mk_stack_prefetch_stats", _c.c_int, [_vp, _vp])
 _lib_mk_stack_destroy = _sig("mk_stack_destroy", None, [_vp])
 _lib_mk_status_string = _sig("mk_status_string", _c.c_char_p, [_c.c_int])
 _lib_mk_layer_get_info = _sig("mk_layer_get_info", _c.c_int, [_vp, _c.POINTER(mk_layer_info)])
@@ -119,6 +127,7 @@ _lib_mk_decode_step_noalloc = _sig("mk_decode_step_noalloc", _c.c_int,
 EXPORTED = ["mk_layer_create", "mk_decode_step", "mk_decode_step_noalloc", "mk_layer_status", "mk_layer_clear_status",
             "mk_layer_destroy", "mk_stack_create", "mk_stack_step", "mk_stack_status",
             "mk_stack_destroy", "mk_status_string", "mk_layer_get_info", "mk_get_timestamps",
+            "mk_layer_prefetch_stats", "mk_stack_prefetch_stats",
             "mk_selftest_quantize", "mk_selftest_mma", "mk_selftest_copy_scratch",
             "mk_selftest_stream", "mk_selftest_issue"]
 
@@ -148,8 +157,9 @@ def mk_status_string(status):
     return _lib_mk_status_string(int(status)).decode()
 
 
-def make_config(wl, flags=0, max_ctx=None, timeout_ns=0, window=None):
-    """mk_layer_config from a workload/layer shape dict."""
+def make_config(wl, flags=0, max_ctx=None, timeout_ns=0, window=None, prefetch_experts=None):
+    """mk_layer_config from a workload/layer shape dict.  prefetch_experts:
+    experts of the previous step prefetched into L2 (MoE; None = 0, off)."""
     c = mk_layer_config()
     c.hidden = wl["hidden"]
     c.n_q_heads = wl["n_q_heads"]
@@ -167,6 +177,9 @@ def make_config(wl, flags=0, max_ctx=None, timeout_ns=0, window=None):
     c.max_ctx = max_ctx if max_ctx is not None else wl["ctx"] + 16
     c.rms_eps = 1e-6
     c.flags = flags
+    if prefetch_experts is None:
+        prefetch_experts = 0
+    c.prefetch_experts = prefetch_experts
     c.wait_timeout_ns = timeout_ns
     return c
 
@@ -250,6 +263,22 @@ def mk_stack_step(stack, io, stream=None):
 
 def mk_stack_status(stack):
     return _lib_mk_stack_status(stack)
+
+
+def _stats_dict(st):
+    return {f: int(getattr(st, f)) for f, _ in mk_prefetch_stats._fields_}
+
+
+def mk_layer_prefetch_stats(layer):
+    st = mk_prefetch_stats()
+    _check("mk_layer_prefetch_stats", _lib_mk_layer_prefetch_stats(layer, ctypes.byref(st)))
+    return _stats_dict(st)
+
+
+def mk_stack_prefetch_stats(stack):
+    st = mk_prefetch_stats()
+    _check("mk_stack_prefetch_stats", _lib_mk_stack_prefetch_stats(stack, ctypes.byref(st)))
+    return _stats_dict(st)
 
 
 def mk_stack_destroy(stack):

@@ -60,6 +60,7 @@ mk_status validate_config(const mk_layer_config* c, const mk_layer_weights* w) {
   if (c->max_tokens < 1 || c->max_tokens > kMaxT) return MK_ERR_UNSUPPORTED;
   if (c->max_ctx < 1) return MK_ERR_INVALID_ARG;
   if (c->flags & ~(MK_FIRST_LAYER | MK_FUSE_NEXT_QKV | MK_TOPK_RENORM)) return MK_ERR_INVALID_ARG;
+  if (c->prefetch_experts < 0 || c->prefetch_experts > kMaxPf) return MK_ERR_INVALID_ARG;
   if (!w->w_qkv && (c->flags & MK_FIRST_LAYER)) return MK_ERR_INVALID_ARG;
   if ((c->flags & MK_FIRST_LAYER) && !w->attn_norm_w) return MK_ERR_INVALID_ARG;
   if (!w->w_o || !w->ffn_norm_w) return MK_ERR_INVALID_ARG;
@@ -255,6 +256,7 @@ mk_status mk_layer_create(const mk_layer_config* cfg, const mk_layer_weights* w,
   P.eps = c.rms_eps;
   P.timeout_ns = c.wait_timeout_ns;
   P.grid = L->sm_count;
+  P.pf_n = P.moe ? std::min(c.prefetch_experts, P.E) : 0;
   P.attn_norm_w = static_cast<const __nv_bfloat16*>(w->attn_norm_w);
   P.ffn_norm_w = static_cast<const __nv_bfloat16*>(w->ffn_norm_w);
   P.next_attn_norm_w = static_cast<const __nv_bfloat16*>(w->next_attn_norm_w);
@@ -326,6 +328,9 @@ mk_status mk_layer_create(const mk_layer_config* cfg, const mk_layer_weights* w,
     MK_TRY(dalloc(L, &P.comb_ctr, T * (P.P / 128)));
     MK_TRY(dalloc(L, &P.exp_sync, 2 * kMaxE));
     MK_TRY(dalloc(L, &P.srow_a, T * kMaxK));
+    MK_TRY(dalloc(L, &P.pf_list, 2 * kMaxPf));
+    MK_CUDA_TRY(cudaMemset(P.pf_list, 0xFF, 2 * kMaxPf * sizeof(int32_t)));  // empty lists
+    MK_TRY(dalloc(L, &P.pf_stats, 4));
     part = std::max(part, static_cast<size_t>(P.ks_rp) * T * (P.tiles_router + P.tiles_pool) * 128);
     part = std::max(part, static_cast<size_t>(P.ks_unpool) * T * P.tiles_unpool * 128);
     uint8_t* sf = nullptr;
@@ -490,6 +495,35 @@ mk_status mk_stack_status(mk_stack* S) {
   return MK_OK;
 }
 
+mk_status mk_layer_prefetch_stats(mk_layer* layer, mk_prefetch_stats* out) {
+  if (!layer || !out) return MK_ERR_INVALID_ARG;
+  std::memset(out, 0, sizeof(*out));
+  const LayerParams& P = layer->tmpl;
+  if (!P.pf_stats) return MK_OK;
+  unsigned long long v[4];
+  MK_CUDA_TRY(cudaMemcpy(v, P.pf_stats, sizeof(v), cudaMemcpyDeviceToHost));
+  out->steps = v[0];
+  out->predicted = v[1];
+  out->active = v[2];
+  out->hits = v[3];
+  return MK_OK;
+}
+
+mk_status mk_stack_prefetch_stats(mk_stack* S, mk_prefetch_stats* out) {
+  if (!S || !out) return MK_ERR_INVALID_ARG;
+  std::memset(out, 0, sizeof(*out));
+  for (mk_layer* L : S->layers) {
+    mk_prefetch_stats s;
+    mk_status st = mk_layer_prefetch_stats(L, &s);
+    if (st != MK_OK) return st;
+    out->steps += s.steps;
+    out->predicted += s.predicted;
+    out->active += s.active;
+    out->hits += s.hits;
+  }
+  return MK_OK;
+}
+
 mk_status mk_get_timestamps(mk_layer* layer, uint64_t* host_buf, size_t n) {
   if (!layer || !host_buf) return MK_ERR_INVALID_ARG;
   const LayerParams& P = layer->tmpl;
@@ -636,6 +670,7 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_layer_config* cfg, const mk
   P.eps = c.rms_eps;
   P.timeout_ns = c.wait_timeout_ns;
   P.grid = D.sm_count;
+  P.pf_n = 0;  // the shared scratch keeps no routing history between calls
   P.attn_norm_w = static_cast<const __nv_bfloat16*>(w->attn_norm_w);
   P.ffn_norm_w = static_cast<const __nv_bfloat16*>(w->ffn_norm_w);
   P.next_attn_norm_w = static_cast<const __nv_bfloat16*>(w->next_attn_norm_w);

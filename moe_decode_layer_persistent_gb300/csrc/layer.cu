@@ -19,7 +19,8 @@
 //   warps 5-6   stagers: wait for a phase's inputs, then write the token
 //               operand (RMSNorm applied, or NVFP4-quantised) into shared
 //               memory in the MMA's swizzled layout.
-//   warp 7      spare (takes part in CTA-wide synchronisation only).
+//   warp 7      spare; in CTA 0 it keeps the expert-prefetch statistics and
+//               the next step's prediction.
 //   warps 8-11  epilogue (TMEM lanes 0-127) and math: split-K fix-ups,
 //               residuals, router top-k, SwiGLU, combine; attention with
 //               warp-level MMA in the attention phase.
@@ -503,6 +504,105 @@ MK_DEV void build_routing(const LayerParams& P, const Smem& S) {
 // ============================================================ producer (warp 0)
 MK_DEV int first_gemm_phase(const LayerParams& P) { return P.first_layer ? PH_QKV : PH_O; }
 
+// L2 prefetch of this CTA's share of the experts the previous step used most
+// (the prediction for this step, by launch parity): per expert the gate, up
+// and down code tiles and their 2 KB scale chunks, spread over the grid.
+MK_DEV void prefetch_predicted_experts(const LayerParams& P) {
+  const uint32_t ep = *reinterpret_cast<const volatile uint32_t*>(P.epoch);
+  // the whole list in one round trip (64 bytes, 16-byte aligned)
+  const int4* l4 = reinterpret_cast<const int4*>(P.pf_list + (ep & 1u) * kMaxPf);
+  int list[kMaxPf];
+#pragma unroll
+  for (int q = 0; q < kMaxPf / 4; ++q) {
+    const int4 v = __ldcg(l4 + q);
+    list[4 * q] = v.x; list[4 * q + 1] = v.y; list[4 * q + 2] = v.z; list[4 * q + 3] = v.w;
+  }
+  const int gt = P.I / 128, gk = (P.P + 255) / 256, dt = P.P / 128, dk = (P.I + 255) / 256;
+  const int ngu = gt * gk, ndn = dt * dk, nmat = 2 * ngu + ndn, per = 2 * nmat;
+#pragma unroll 1
+  for (int k = 0; k < P.pf_n; ++k) {
+    int e = -1;
+#pragma unroll
+    for (int q = 0; q < kMaxPf; ++q)
+      if (q == k) e = list[q];
+    if (e < 0 || e >= P.E) break;
+    const int start = ((static_cast<int>(blockIdx.x) - (k * per) % P.grid) % P.grid + P.grid) % P.grid;
+    for (int i = start; i < per; i += P.grid) {
+      const bool sf = i >= nmat;
+      int j = sf ? i - nmat : i;
+      const CUtensorMap* map;
+      const uint8_t* sfp;
+      int row, x;
+      if (j < 2 * ngu) {  // gate or up
+        const bool up = j >= ngu;
+        j -= up ? ngu : 0;
+        const int rt = j / gk, kb = j % gk;
+        map = up ? &P.tm_up : &P.tm_gate;
+        sfp = (up ? P.sf_up : P.sf_gate) + ((static_cast<size_t>(e) * gt + rt) * gk + kb) * kSfBytes;
+        row = e * P.I + rt * 128;
+        x = kb * 128;
+      } else {            // down
+        j -= 2 * ngu;
+        const int rt = j / dk, kb = j % dk;
+        map = &P.tm_down;
+        sfp = P.sf_down + ((static_cast<size_t>(e) * dt + rt) * dk + kb) * kSfBytes;
+        row = e * P.P + rt * 128;
+        x = kb * 128;
+      }
+      if (sf) bulk_prefetch_l2(sfp, kSfBytes);
+      else tma_prefetch_2d(map, x, row);
+    }
+  }
+}
+
+// Warp 7 of CTA 0, once the routing is known: how many of this step's
+// prefetched experts were routed to, and the next step's prediction (the
+// experts with the most tokens, an equal count going to the lower index).
+MK_DEV void prefetch_bookkeeping(const LayerParams& P, const Smem& S, uint32_t epoch) {
+  Misc* m = S.m;
+  if (!wait_bar(P, S, &m->route_ready, 0, ERR_TIMEOUT_ROUTE)) return;
+  const int lane = lane_id();
+  const int32_t* cur = P.pf_list + (epoch & 1u) * kMaxPf;
+  int32_t* nxt = P.pf_list + ((epoch + 1u) & 1u) * kMaxPf;
+  uint32_t pred = 0, hit = 0;
+  if (lane < P.pf_n) {
+    const int e = cur[lane];
+    if (e >= 0 && e < P.E) {
+      pred = 1;
+      hit = m->off[e + 1] > m->off[e] ? 1u : 0u;
+    }
+  }
+  pred = __reduce_add_sync(0xffffffffu, pred);
+  hit = __reduce_add_sync(0xffffffffu, hit);
+  if (lane == 0) {
+    atomicAdd(P.pf_stats + 0, 1ull);
+    atomicAdd(P.pf_stats + 1, static_cast<unsigned long long>(pred));
+    atomicAdd(P.pf_stats + 2, static_cast<unsigned long long>(m->n_act));
+    atomicAdd(P.pf_stats + 3, static_cast<unsigned long long>(hit));
+  }
+  uint32_t key[kMaxE / 32];
+#pragma unroll
+  for (int i = 0; i < kMaxE / 32; ++i) {
+    const int e = lane + 32 * i;
+    const int c = e < P.E ? m->off[e + 1] - m->off[e] : 0;
+    key[i] = c > 0 ? (static_cast<uint32_t>(c) << 16) | (0xFFFFu - e) : 0u;
+  }
+#pragma unroll 1
+  for (int r = 0; r < kMaxPf; ++r) {
+    uint32_t b = 0u;
+#pragma unroll
+    for (int i = 0; i < kMaxE / 32; ++i) b = max(b, key[i]);
+    const uint32_t wk = r < P.pf_n ? __reduce_max_sync(0xffffffffu, b) : 0u;
+    const int e = wk ? static_cast<int>(0xFFFFu - (wk & 0xFFFFu)) : -1;
+    if (lane == 0) nxt[r] = e;
+    if (e >= 0 && (e & 31) == lane) {
+#pragma unroll
+      for (int i = 0; i < kMaxE / 32; ++i)
+        if (i == (e >> 5)) key[i] = 0u;
+    }
+  }
+}
+
 // L2 prefetch of this CTA's 1/grid share of a bf16 weight matrix [N][K]
 // (128-row x 64-column tiles of its tensor map).
 MK_DEV void prefetch_share_l2(const LayerParams& P, const CUtensorMap* map, int N, int K) {
@@ -524,6 +624,13 @@ MK_DEV void run_producer(const LayerParams& P, const Smem& S) {
       // HBM idles while the router picks the experts: fetch this CTA's share
       // of the weights that do not depend on the routing (unpooler, fused
       // next-layer QKV) into L2 meanwhile
+      if (P.pf_n > 0) {
+        if (!prev_done) {
+          pdl_wait();
+          prev_done = true;
+        }
+        prefetch_predicted_experts(P);
+      }
       prefetch_share_l2(P, &P.tm_unpool, P.H, P.P);
       if (P.fuse_next) prefetch_share_l2(P, &P.tm_nqkv, P.Nqkv, P.H);
       if (!wait_bar(P, S, &m->route_ready, 0, ERR_TIMEOUT_ROUTE)) { ok = false; break; }
@@ -1814,6 +1921,8 @@ __global__ void __launch_bounds__(kThreads, 1) mk_layer_kernel(const __grid_cons
       run_stager(P, S, epoch);
     } else if (warp >= 8) {
       run_epilogue(P, S, epoch);
+    } else if (warp == 7 && blockIdx.x == 0 && P.pf_n > 0) {
+      prefetch_bookkeeping(P, S, epoch);
     }
   }
   tc_fence_before();

@@ -15,6 +15,7 @@ constexpr int kMaxE = 256;
 constexpr int kMaxK = 8;          // top-k
 constexpr int kTmemCols = 512;
 constexpr int kNumCounters = 16;  // grid-wide dependency counters
+constexpr int kMaxPf = 16;        // experts prefetched from the previous step, at most
 
 // Phases of one launch, in order.
 enum PhaseId : int {
@@ -115,6 +116,9 @@ struct LayerParams {
   float* srow_a;            // MoE: NVFP4 row scales of the SwiGLU rows [16*k]
   uint32_t* misc_ctr;       // [0]: router tiles done
   uint32_t* sched;          // [PH_COUNT] next unclaimed unit of each phase (reset by CTA 0 at the end)
+  int pf_n;                 // MoE: experts prefetched from the previous step (0: off)
+  int32_t* pf_list;         // [2][kMaxPf] predicted experts by launch parity, -1 ends a list
+  unsigned long long* pf_stats;  // [4] steps, predicted, active, hits
   uint32_t* bar_ctr;        // [kNumCounters] grid dependency counters
   uint32_t* epoch;          // launches of this layer so far
   uint32_t* status;         // sticky error word

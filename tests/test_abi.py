@@ -80,10 +80,20 @@ def test_create_rejects_bad_arguments_without_a_gpu(lib):
     with pytest.raises(b.MkError) as e:
         b.mk_layer_create(c3, fake)
     assert e.value.status == 1
+    # expert prefetch count outside 0..16
+    for n in (-1, 17):
+        c4 = b.make_config(wl, flags=b.MK_FIRST_LAYER, prefetch_experts=n)
+        with pytest.raises(b.MkError) as e:
+            b.mk_layer_create(c4, fake)
+        assert e.value.status == 1, n
 
 
 def test_null_handles(lib):
     from moe_decode_layer_persistent_gb300 import binding as b
+    with pytest.raises(b.MkError):
+        b.mk_layer_prefetch_stats(None)
+    with pytest.raises(b.MkError):
+        b.mk_stack_prefetch_stats(None)
     io = b.make_step_io(1, 0, 0, 0, 0, 0)
     with pytest.raises(b.MkError):
         b.mk_decode_step(None, io)

@@ -111,6 +111,50 @@ def test_repeated_steps_and_determinism(cuda_lib):
     cuda_lib.mk_layer_destroy(layer)
 
 
+def _predicted(idx_prev, n, E):
+    """The previous step's n most-used experts, an equal count going to the
+    lower index (experts with no token are never predicted)."""
+    cnt = np.bincount(np.asarray(idx_prev).ravel(), minlength=E)
+    order = sorted(range(E), key=lambda e: (-cnt[e], e))
+    return [e for e in order[:n] if cnt[e] > 0]
+
+
+def test_expert_prefetch_statistics(cuda_lib):
+    """Each step prefetches the previous step's most-used experts; the layer
+    counts steps, predicted, active and hit experts.  The host recomputes the
+    prediction from the previous step's top-k indices."""
+    N = 5
+    work, Wn = H.prepare("tiny_layer", "host", T=16, ctx=60)
+    other = synth.make_workload("tiny_layer", device="cpu", T=16, ctx=60, seed=synth.SEED_BASE + 77)
+    c = work["cfgs"][0]
+    E, k = c["n_experts"], c["top_k"]
+    kc, vc = (t.clone() for t in work["caches"][0])
+    cfg = cuda_lib.make_config(c, flags=cuda_lib.MK_FIRST_LAYER, max_ctx=kc.shape[0], prefetch_experts=N)
+    layer = cuda_lib.mk_layer_create(cfg, work["Ws"][0])
+    xs = [work["x_in"], work["x_in"], other["x_in"][:16].to("cuda")]
+    idxs = []
+    for x in xs:
+        x_out = torch.zeros_like(x)
+        idx = torch.full((16, k), -1, dtype=torch.int32, device="cuda")
+        io = cuda_lib.make_step_io(16, 60, x.contiguous(), x_out, kc, vc, topk_idx_out=idx)
+        cuda_lib.mk_decode_step(layer, io)
+        torch.cuda.synchronize()
+        idxs.append(idx.cpu().numpy())
+    assert cuda_lib.mk_layer_status(layer) == 0
+    st = cuda_lib.mk_layer_prefetch_stats(layer)
+    cuda_lib.mk_layer_destroy(layer)
+    want = dict(steps=3, predicted=0, active=0, hits=0)
+    for s, idx in enumerate(idxs):
+        active = set(idx.ravel().tolist())
+        want["active"] += len(active)
+        if s > 0:
+            pred = _predicted(idxs[s - 1], N, E)
+            want["predicted"] += len(pred)
+            want["hits"] += len(active & set(pred))
+    assert st == want, (st, want)
+    assert st["hits"] >= len(_predicted(idxs[0], N, E))  # step 2 repeats step 1's routing
+
+
 def test_bounded_wait_reports_timeout_and_recovers(cuda_lib):
     """A wait limit of 1 ns makes the first wait that is not already satisfied
     give up: the kernel returns, the status reads MK_ERR_TIMEOUT, the context
