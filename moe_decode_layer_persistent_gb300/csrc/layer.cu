@@ -1728,23 +1728,45 @@ MK_DEV void combine_phase_end(const LayerParams& P, const Smem& S, int et) {
     }
   }
   epi_sync();
+  // 16 threads per completed (token, tile) pair, 8 features each with 16-byte
+  // loads: 8 pairs at a time; each feature sums its k terms in rank order
   const int nd = m->n_done;
-  for (int d = 0; d < nd; ++d) {
+  for (int d0 = 0; d0 < nd; d0 += 8) {
+    const int d = d0 + (et >> 4);
+    if (d >= nd) continue;
     const int i = m->done_pairs[d];
-    const int t = i / tiles, f = (i % tiles) * 128 + et;
-    float z[kMaxK], wr[kMaxK];
+    const int t = i / tiles, f0 = (i % tiles) * 128 + (et & 15) * 8;
+    uint4 z[kMaxK];
+    float wr[kMaxK];
 #pragma unroll
     for (int r = 0; r < kMaxK; ++r) {
       if (r < P.topk) {
-        z[r] = ld_bf(P.z_buf + static_cast<size_t>(t * P.topk + r) * P.P + f);
+        z[r] = __ldcg(reinterpret_cast<const uint4*>(P.z_buf + static_cast<size_t>(t * P.topk + r) * P.P + f0));
         wr[r] = __ldcg(P.wts + t * P.topk + r);
       }
     }
-    float acc = 0.f;
+    float acc[8];
 #pragma unroll
-    for (int r = 0; r < kMaxK; ++r)
-      if (r < P.topk) acc += wr[r] * z[r];
-    P.y_buf[static_cast<size_t>(t) * P.P + f] = to_bf(acc);
+    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+#pragma unroll
+    for (int r = 0; r < kMaxK; ++r) {
+      if (r < P.topk) {
+        const uint32_t* zw = reinterpret_cast<const uint32_t*>(&z[r]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc[2 * j] += wr[r] * __uint_as_float(zw[j] << 16);
+          acc[2 * j + 1] += wr[r] * __uint_as_float(zw[j] & 0xFFFF0000u);
+        }
+      }
+    }
+    uint4 o;
+    uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
+      ow[j] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(P.y_buf + static_cast<size_t>(t) * P.P + f0) = o;
   }
 }
 
