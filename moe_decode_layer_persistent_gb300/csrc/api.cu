@@ -51,6 +51,43 @@ int choose_ksplit(int K) {
   return nkb;
 }
 
+// QKV output rows of KV-head group g: its 4 q heads, its k head, its v head.
+bool tile_holds_group(const LayerParams& P, int tile, int g) {
+  const int a = tile * 128, b = a + 128;
+  auto hit = [&](int lo, int n) { return lo < b && lo + n > a; };
+  return hit(g * 4 * P.d, 4 * P.d) || hit(P.Hq * P.d + g * P.d, P.d) ||
+         hit(P.Hq * P.d + P.Hkv * P.d + g * P.d, P.d);
+}
+
+// QKV tiles in claim order, group by group (so that each group's q, k and v
+// rows are finished early and its attention can start), and the number of
+// tiles each group waits for.
+void qkv_group_order(LayerParams& P) {
+  for (int i = 0; i < 64; ++i) P.qkv_order[i] = static_cast<uint8_t>(i);
+  for (int g = 0; g < kMaxGroups; ++g) P.grp_tiles[g] = 0;
+  if (P.tiles_qkv > 256) return;  // rejected by the shape checks
+  bool taken[256] = {};
+  int order[256];
+  int n = 0;
+  for (int g = 0; g < P.Hkv; ++g) {
+    P.grp_tiles[g] = 0;
+    for (int t = 0; t < P.tiles_qkv; ++t) {
+      if (!tile_holds_group(P, t, g)) continue;
+      ++P.grp_tiles[g];
+      if (!taken[t]) {
+        taken[t] = true;
+        order[n++] = t;
+      }
+    }
+  }
+  for (int t = 0; t < P.tiles_qkv; ++t)
+    if (!taken[t]) order[n++] = t;
+  // the kernel reorders the first 64 tiles (wider QKV projections keep their
+  // order: readiness is counted per tile either way)
+  if (P.tiles_qkv <= 64)
+    for (int i = 0; i < P.tiles_qkv; ++i) P.qkv_order[i] = static_cast<uint8_t>(order[i]);
+}
+
 mk_status validate_config(const mk_layer_config* c, const mk_layer_weights* w) {
   if (!c || !w) return MK_ERR_INVALID_ARG;
   if (c->hidden <= 0 || c->hidden % 256) return MK_ERR_UNSUPPORTED;
@@ -61,6 +98,7 @@ mk_status validate_config(const mk_layer_config* c, const mk_layer_weights* w) {
   if (c->max_ctx < 1) return MK_ERR_INVALID_ARG;
   if (c->flags & ~(MK_FIRST_LAYER | MK_FUSE_NEXT_QKV | MK_TOPK_RENORM)) return MK_ERR_INVALID_ARG;
   if (c->prefetch_experts < 0 || c->prefetch_experts > kMaxPf) return MK_ERR_INVALID_ARG;
+  if (c->n_kv_heads > kMaxGroups) return MK_ERR_UNSUPPORTED;
   if (!w->w_qkv && (c->flags & MK_FIRST_LAYER)) return MK_ERR_INVALID_ARG;
   if ((c->flags & MK_FIRST_LAYER) && !w->attn_norm_w) return MK_ERR_INVALID_ARG;
   if (!w->w_o || !w->ffn_norm_w) return MK_ERR_INVALID_ARG;
@@ -264,6 +302,7 @@ mk_status mk_layer_create(const mk_layer_config* cfg, const mk_layer_weights* w,
   // split-K geometry
   P.ks_qkv = choose_ksplit(P.H);
   P.tiles_qkv = (P.Nqkv + 127) / 128;
+  qkv_group_order(P);
   P.ks_o = choose_ksplit(P.Hq * P.d);
   P.tiles_o = P.H / 128;
   P.ks_rp = choose_ksplit(P.H);
@@ -349,12 +388,14 @@ mk_status mk_layer_create(const mk_layer_config* cfg, const mk_layer_weights* w,
     part = std::max(part, static_cast<size_t>(P.ks_ddown) * T * P.tiles_ddown * 128);
   }
   MK_TRY(dalloc(L, &P.part, part));
+  MK_TRY(dalloc(L, &P.part_o, static_cast<size_t>(P.ks_o) * T * P.tiles_o * 128));
   L->attn_max_chunks = std::max(1, L->sm_count / P.Hkv);
   MK_TRY(dalloc(L, &P.attn_part,
                 static_cast<size_t>(P.Hkv) * L->attn_max_chunks * 64 * (P.d + 2)));
   MK_TRY(dalloc(L, &P.fix_ctr, static_cast<size_t>(PH_COUNT) * 256));
   MK_TRY(dalloc(L, &P.misc_ctr, 4));
   MK_TRY(dalloc(L, &P.sched, PH_COUNT));
+  MK_TRY(dalloc(L, &P.grp_sync, 6 * kMaxGroups));
   MK_TRY(dalloc(L, &P.bar_ctr, kNumCounters));
   MK_TRY(dalloc(L, &P.epoch, 1));
   MK_TRY(dalloc(L, &P.status, 1));
@@ -396,6 +437,7 @@ mk_status mk_layer_clear_status(mk_layer* layer) {
   MK_CUDA_TRY(cudaMemset(P.fix_ctr, 0, PH_COUNT * 256 * sizeof(uint32_t)));
   MK_CUDA_TRY(cudaMemset(P.misc_ctr, 0, 4 * sizeof(uint32_t)));
   MK_CUDA_TRY(cudaMemset(P.sched, 0, PH_COUNT * sizeof(uint32_t)));
+  MK_CUDA_TRY(cudaMemset(P.grp_sync, 0, 6 * kMaxGroups * sizeof(uint32_t)));
   if (P.comb_ctr)
     MK_CUDA_TRY(cudaMemset(P.comb_ctr, 0, kMaxT * (P.P / 128) * sizeof(uint32_t)));
   if (P.exp_sync) MK_CUDA_TRY(cudaMemset(P.exp_sync, 0, 2 * kMaxE * sizeof(uint32_t)));
@@ -676,6 +718,7 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_layer_config* cfg, const mk
   P.next_attn_norm_w = static_cast<const __nv_bfloat16*>(w->next_attn_norm_w);
   P.ks_qkv = choose_ksplit(P.H);
   P.tiles_qkv = (P.Nqkv + 127) / 128;
+  qkv_group_order(P);
   P.ks_o = choose_ksplit(P.Hq * P.d);
   P.tiles_o = P.H / 128;
   P.ks_rp = choose_ksplit(P.H);
@@ -758,10 +801,12 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_layer_config* cfg, const mk
     part = std::max(part, static_cast<size_t>(P.ks_ddown) * T * P.tiles_ddown * 128);
   }
   P.part = cv.take<float>(part);
+  P.part_o = cv.take<float>(static_cast<size_t>(P.ks_o) * T * P.tiles_o * 128);
   L.attn_max_chunks = std::min(kNoAllocMaxChunks, std::max(1, D.sm_count / P.Hkv));
   P.attn_part = cv.take<float>(static_cast<size_t>(P.Hkv) * L.attn_max_chunks * 64 * (P.d + 2));
   // counters that must start at zero each call: one contiguous block
-  uint32_t* zero = cv.take<uint32_t>(static_cast<size_t>(PH_COUNT) * 256 + 4 + kNumCounters + 2 + PH_COUNT);
+  uint32_t* zero = cv.take<uint32_t>(static_cast<size_t>(PH_COUNT) * 256 + 4 + kNumCounters + 2 + PH_COUNT +
+                                     6 * kMaxGroups);
   if (cv.overflow) {
     if (log_enabled())
       std::fprintf(stderr, "mk: mk_decode_step_noalloc: this layer needs more than the %zu-byte scratch\n",
@@ -774,6 +819,7 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_layer_config* cfg, const mk
   P.epoch = P.bar_ctr + kNumCounters;
   P.status = P.epoch + 1;
   P.sched = P.status + 1;
+  P.grp_sync = P.sched + PH_COUNT;
   P.ts = nullptr;
 
   // per-step fields and the attention split (same rules as mk_decode_step,
@@ -783,7 +829,8 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_layer_config* cfg, const mk
   if (st != MK_OK) return st;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  MK_CUDA_TRY(cudaMemsetAsync(zero, 0, (static_cast<size_t>(PH_COUNT) * 256 + 4 + kNumCounters + 2 + PH_COUNT) * 4, s));
+  MK_CUDA_TRY(cudaMemsetAsync(zero, 0, (static_cast<size_t>(PH_COUNT) * 256 + 4 + kNumCounters + 2 + PH_COUNT +
+                                        6 * kMaxGroups) * 4, s));
   if (P.comb_ctr) MK_CUDA_TRY(cudaMemsetAsync(P.comb_ctr, 0, T * (P.P / 128) * 4, s));
   if (P.exp_sync) MK_CUDA_TRY(cudaMemsetAsync(P.exp_sync, 0, 2 * kMaxE * 4, s));
   if (P.moe) {

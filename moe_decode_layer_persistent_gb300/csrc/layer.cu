@@ -59,6 +59,7 @@ struct Misc {
   uint64_t route_ready;
   uint64_t mma_done;
   uint64_t land[2][3];             // stager landing copies per operand buffer: [0] bf16 rows, [1..2] per-warp rows
+  uint64_t attn_free;              // the epilogue's attention no longer uses the operand buffers
   uint64_t uq_full[8];             // unit queue: slot written by the producer
   uint64_t uq_empty[8];            // unit queue: slot read by the 4 MMA issuers, stager and epilogue leaders
   uint32_t tmem_base;
@@ -97,7 +98,7 @@ struct Smem {
 enum : uint32_t {
   ERR_TIMEOUT_FULL = 0x100, ERR_TIMEOUT_EMPTY = 0x200, ERR_TIMEOUT_B = 0x300,
   ERR_TIMEOUT_ACC = 0x400, ERR_TIMEOUT_GRID = 0x500, ERR_TIMEOUT_ROUTE = 0x600,
-  ERR_TIMEOUT_EXPERT = 0x700, ERR_TIMEOUT_QUEUE = 0x800
+  ERR_TIMEOUT_DATA = 0x700, ERR_TIMEOUT_QUEUE = 0x800
 };
 
 MK_DEV bool aborted(const LayerParams& P, const Smem& S) {
@@ -205,11 +206,39 @@ MK_DEV bool group_grid_wait(const LayerParams& P, const Smem& S, int id, uint32_
 }
 MK_DEV bool group_flag_wait(const LayerParams& P, const Smem& S, const uint32_t* f, uint32_t value,
                             bool leader, int bar_id, int n, int slot) {
-  if (leader) S.m->grp_ok[slot] = flag_wait(P, S, f, value, ERR_TIMEOUT_EXPERT) ? 1 : 0;
+  if (leader) S.m->grp_ok[slot] = flag_wait(P, S, f, value, ERR_TIMEOUT_DATA) ? 1 : 0;
   named_bar(bar_id, n);
   const bool ok = *reinterpret_cast<volatile int*>(&S.m->grp_ok[slot]) != 0;
   named_bar(bar_id, n);
   return ok;
+}
+
+// ------------------------------------------------------------ per-group dataflow
+// QKV -> attention -> merge -> o-proj proceed per KV-head group g: kind 0
+// counts g's finished QKV tiles, 1 its attention chunks, 2 its merged
+// (token, head) items; the last arrival resets the counter and releases the
+// kind's ready flag with the launch's epoch + 1.
+MK_DEV uint32_t* grp_ctr(const LayerParams& P, int kind, int g) { return P.grp_sync + kind * kMaxGroups + g; }
+MK_DEV uint32_t* grp_flag(const LayerParams& P, int kind, int g) {
+  return P.grp_sync + (3 + kind) * kMaxGroups + g;
+}
+// One thread, after the data it counts is written and fenced.
+MK_DEV void grp_count_in(const LayerParams& P, int kind, int g, uint32_t need, uint32_t epoch) {
+  uint32_t* c = grp_ctr(P, kind, g);
+  if (atomicAdd(c, 1u) == need - 1u) {
+    *c = 0;
+    __threadfence();
+    st_release(grp_flag(P, kind, g), epoch + 1u);
+  }
+}
+MK_DEV bool grp_ready(const LayerParams& P, int kind, int g, uint32_t epoch) {
+  return static_cast<int32_t>(ld_acquire(grp_flag(P, kind, g)) - (epoch + 1u)) >= 0;
+}
+// Does QKV tile t hold rows of group g (its 4 q heads, its k and v heads)?
+MK_DEV bool tile_in_group(const LayerParams& P, int t, int g) {
+  const int a = t * 128, b = a + 128;
+  const int q0 = g * 4 * P.d, k0 = P.Hq * P.d + g * P.d, v0 = k0 + P.Hkv * P.d;
+  return (q0 < b && q0 + 4 * P.d > a) || (k0 < b && k0 + P.d > a) || (v0 < b && v0 + P.d > a);
 }
 
 // ------------------------------------------------------------ unit queue
@@ -308,7 +337,7 @@ MK_DEV int first_unit(const LayerParams& P, int ph) {
 // The grid counter a phase's token operand waits for (-1: none).
 MK_DEV int phase_dep(const LayerParams& P, int ph) {
   switch (ph) {
-    case PH_O: return BAR_MERGE;
+    case PH_O: return -1;  // per group of merged heads (grp_sync)
     case PH_RP: return BAR_O;
     case PH_GU: return BAR_RP;
     case PH_DOWN: return P.moe ? -1 : BAR_RP;  // MoE: per expert (exp_sync)
@@ -362,8 +391,15 @@ MK_DEV Unit make_unit(const LayerParams& P, const Smem& S, int ph, int u) {
     U.map[0] = m;
     U.fp4 = 0;
     U.col_tile = u / ks_count;
-    U.tile = U.col_tile - tile_base;
     U.ks = u % ks_count;
+    if (ph == PH_QKV || ph == PH_NQKV) {
+      U.col_tile = u / ks_count < 64 ? P.qkv_order[u / ks_count] : u / ks_count;  // group by group
+    } else if (ph == PH_O) {
+      // K-slice by K-slice: each slice is one group's merged heads
+      U.col_tile = u % P.tiles_o;
+      U.ks = u / P.tiles_o;
+    }
+    U.tile = U.col_tile - tile_base;
     U.ksplit = ks_count;
     U.row0 = U.tile * 128;
     const int kc = K / ks_count;
@@ -442,6 +478,12 @@ MK_DEV Unit make_unit(const LayerParams& P, const Smem& S, int ph, int u) {
     }
   }
   return U;
+}
+
+// o-proj unit: the groups whose heads its K-slice of o covers.
+MK_DEV int o_group_lo(const LayerParams& P, const Unit& U) { return U.x0 / (4 * P.d); }
+MK_DEV int o_group_hi(const LayerParams& P, const Unit& U) {
+  return (U.x0 + U.nkb * 64 - 1) / (4 * P.d);
 }
 
 // ------------------------------------------------------------ routing table
@@ -1013,16 +1055,32 @@ MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
     stage_sync();
     // expert down units wait for their own expert's gate/up tiles, not for
     // the whole phase: their rows are copied ahead only once it is ready
-    const bool per_expert = ph == PH_DOWN && P.moe;
+    // units that wait for their own inputs instead of a whole phase: expert
+    // down (its expert's gate/up tiles), o-proj (its K-slice's head groups)
+    const bool per_unit = (ph == PH_DOWN && P.moe) || ph == PH_O;
+    auto unit_ready = [&](const Unit& V) -> bool {  // non-blocking (leader)
+      if (ph == PH_O) {
+        for (int g = o_group_lo(P, V); g <= o_group_hi(P, V); ++g)
+          if (!grp_ready(P, 2, g, epoch)) return false;
+        return true;
+      }
+      return static_cast<int32_t>(ld_acquire(P.exp_sync + kMaxE + V.expert) - (epoch + 1u)) >= 0;
+    };
     // The leader copies a unit's first inputs ahead into the buffer's landing
     // area and records whether it did (read by all after the next barrier).
     auto try_prefetch = [&](const Unit& V, int buf) {
       if (tid != 0) return;
-      const bool ready = !per_expert ||
-          static_cast<int32_t>(ld_acquire(P.exp_sync + kMaxE + V.expert) - (epoch + 1u)) >= 0;
+      const bool ready = !per_unit || unit_ready(V);
       if (ready) prefetch_unit(P, S, ph, V, buf);
       m->pref_ok[buf] = ready ? 1 : 0;
     };
+    // attention keeps its tiles in the operand buffers: the o-proj (which no
+    // longer waits for every head group) starts once this CTA's attention is done
+    if (ph == PH_O &&
+        !group_mbar_wait(P, S, &m->attn_free, 0, ERR_TIMEOUT_B, tid == 0, kBarStage, 64, 0)) {
+      ok = false;
+      break;
+    }
     // the phase's first unit, its inputs copied at once; later units' are
     // copied one unit ahead when the producer has already claimed them
     int u;
@@ -1046,12 +1104,15 @@ MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
         break;
       }
       const bool pre = *reinterpret_cast<volatile int*>(&m->pref_ok[b]) != 0;
-      if (per_expert && !pre) {
-        // not ready when looked at ahead: wait for the expert now
-        if (!group_flag_wait(P, S, P.exp_sync + kMaxE + U.expert, epoch + 1u, tid == 0, kBarStage, 64, 0)) {
-          ok = false;
-          break;
+      if (per_unit && !pre) {
+        // not ready when looked at ahead: wait for the unit's inputs now
+        if (ph == PH_O) {
+          for (int g = o_group_lo(P, U); g <= o_group_hi(P, U) && ok; ++g)
+            ok = group_flag_wait(P, S, grp_flag(P, 2, g), epoch + 1u, tid == 0, kBarStage, 64, 0);
+        } else {
+          ok = group_flag_wait(P, S, P.exp_sync + kMaxE + U.expert, epoch + 1u, tid == 0, kBarStage, 64, 0);
         }
+        if (!ok) break;
       }
       const uint64_t w1 = tnow(P);
       bool sok = true;
@@ -1368,12 +1429,14 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
 
   // bf16 phase: split-K partials + fix-up by the last arriving unit of a tile
   if (U.ksplit > 1) {
+    // the o-proj overlaps the QKV phase (per head group), so it has its own
+    float* part = ph == PH_O ? P.part_o : P.part;
     // partials: part[ks][j][col][16 tokens], col = col_tile * 128 + row in
     // tile: each thread moves its 16 token values as four 16-byte vectors
     const size_t ncol = static_cast<size_t>(U.col_tiles) * 128;
     const int col = U.col_tile * 128 + et;
     for (int j = 0; j < U.pair; ++j) {
-      float4* dst = reinterpret_cast<float4*>(P.part + ((static_cast<size_t>(U.ks * U.pair + j)) * ncol + col) * kMaxT);
+      float4* dst = reinterpret_cast<float4*>(part + ((static_cast<size_t>(U.ks * U.pair + j)) * ncol + col) * kMaxT);
       const float* v = j ? u : g;
 #pragma unroll
       for (int q = 0; q < 4; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
@@ -1402,7 +1465,7 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
         for (int kk = 0; kk < 4; ++kk) {
           if (ks + kk < U.ksplit) {
             const float4* src = reinterpret_cast<const float4*>(
-                P.part + ((static_cast<size_t>((ks + kk) * U.pair + j)) * ncol + col) * kMaxT);
+                part + ((static_cast<size_t>((ks + kk) * U.pair + j)) * ncol + col) * kMaxT);
 #pragma unroll
             for (int q = 0; q < 4; ++q) v[kk][q] = __ldcg(src + q);
           }
@@ -1425,6 +1488,15 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
     }
   }
   epi_bf16_final(P, S, ph, U, et, g, u);
+  if (ph == PH_QKV) {
+    // this tile's q, k and v rows are final: count it in for its groups
+    epi_sync();
+    if (et == 0) {
+      __threadfence();
+      for (int gg = 0; gg < P.Hkv; ++gg)
+        if (tile_in_group(P, U.tile, gg)) grp_count_in(P, 0, gg, P.grp_tiles[gg], m->epoch);
+    }
+  }
   if (ph == PH_RP && P.moe && U.router) {
     // the last finished router tile computes the top-k for every token
     epi_sync();
@@ -1499,6 +1571,8 @@ template <int D>
 MK_DEV void attention_unit(const LayerParams& P, const Smem& S, int g, int lo, int hi, int chunk_id,
                            int et) {
   constexpr int kChunks = D / 8;  // 16-byte chunks per row
+  // Q and the double-buffered K/V tiles live in the two operand buffers (80 KB):
+  // the stagers stay out of them until the epilogue arrives on attn_free
   uint8_t* sQ = S.bbuf(0);
   uint8_t* sK[2] = {sQ + 64 * D * 2, sQ + 64 * D * 2 + 2 * 64 * D * 2};
   uint8_t* sV[2] = {sK[0] + 64 * D * 2, sK[1] + 64 * D * 2};
@@ -1797,29 +1871,58 @@ MK_DEV void run_epilogue(const LayerParams& P, const Smem& S, uint32_t epoch) {
     if (ph == last_ph && et == 0) pdl_launch_dependents();
     if (et == 0) stamp(P, S, ph, 0);
     if (ph == PH_ATTN) {
-      if (P.first_layer && !(ok = epi_wait(P, S, BAR_QKV, target, et))) break;
+      // a chunk of KV head g waits only for g's q, k and v rows
       const int n = phase_units(P, S, ph);
-      for (int u = first_unit(P, ph); u < n; u += P.grid) {
+      for (int u = first_unit(P, ph); u < n && ok; u += P.grid) {
         const int g = u / P.attn_chunks, c = u % P.attn_chunks;
+        if (P.first_layer &&
+            !(ok = group_flag_wait(P, S, grp_flag(P, 0, g), epoch + 1u, et == 0, kBarEpi, 128, 1)))
+          break;
         const int lo = P.attn_lo + c * P.attn_chunk_len;
         const int hi = min(P.ctx + P.T, lo + P.attn_chunk_len);
         if (P.d == 128) attention_unit<128>(P, S, g, lo, hi, c, et);
         else attention_unit<64>(P, S, g, lo, hi, c, et);
+        epi_sync();
+        if (et == 0) {
+          __threadfence();
+          grp_count_in(P, 1, g, P.attn_chunks, epoch);
+        }
       }
-      if (et == 0) stamp(P, S, ph, 1);
+      if (!ok) break;
+      if (et == 0) {
+        stamp(P, S, ph, 1);
+        mbar_arrive(&m->attn_free);  // the o-proj stagers may now use the operand buffers
+      }
       epi_arrive(P, S, BAR_ATTN, et);
       continue;
     }
     if (ph == PH_MERGE) {
-      if (!(ok = epi_wait(P, S, BAR_ATTN, target, et))) break;
+      // an item (token, q head) waits only for its group's chunks
       const int n = phase_units(P, S, ph);
       const int w = et >> 5;
       int k = 0;
-      for (int u = first_unit(P, ph); u < n; u += P.grid, ++k) {
+      bool wok = true;
+      for (int u = first_unit(P, ph); u < n && wok; u += P.grid, ++k) {
         if ((k & 3) != w) continue;  // the CTA's k-th item goes to warp k % 4
+        const int g = (u % P.Hq) / 4;
+        int r = 1;
+        if (lane_id() == 0) r = flag_wait(P, S, grp_flag(P, 1, g), epoch + 1u, ERR_TIMEOUT_DATA) ? 1 : 0;
+        if (!(wok = __shfl_sync(0xffffffffu, r, 0) != 0)) break;
+        __syncwarp();  // the lanes' loads below follow lane 0's acquire
         if (P.d == 128) merge_item<128>(P, u);
         else merge_item<64>(P, u);
+        __syncwarp();
+        if (lane_id() == 0) {
+          __threadfence();
+          grp_count_in(P, 2, g, static_cast<uint32_t>(P.T * 4), epoch);
+        }
       }
+      // the epilogue warps agree on the outcome before their next barrier
+      if (lane_id() == 0) m->red[0][w] = wok ? 1.f : 0.f;
+      epi_sync();
+      ok = m->red[0][0] != 0.f && m->red[0][1] != 0.f && m->red[0][2] != 0.f && m->red[0][3] != 0.f;
+      epi_sync();
+      if (!ok) break;
       if (et == 0) stamp(P, S, ph, 1);
       epi_arrive(P, S, BAR_MERGE, et);
       continue;
@@ -1906,6 +2009,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_layer_kernel(const __grid_cons
     }
     mbar_init(&m->route_ready, 1);
     mbar_init(&m->mma_done, 4);
+    mbar_init(&m->attn_free, 1);
     for (int i = 0; i < kUQ; ++i) {
       mbar_init(&m->uq_full[i], 1);
       mbar_init(&m->uq_empty[i], 6);  // 4 MMA issuers, stager and epilogue leaders

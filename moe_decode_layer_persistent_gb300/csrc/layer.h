@@ -16,6 +16,7 @@ constexpr int kMaxK = 8;          // top-k
 constexpr int kTmemCols = 512;
 constexpr int kNumCounters = 16;  // grid-wide dependency counters
 constexpr int kMaxPf = 16;        // experts prefetched from the previous step, at most
+constexpr int kMaxGroups = 16;    // KV heads (GQA groups), at most
 
 // Phases of one launch, in order.
 enum PhaseId : int {
@@ -134,6 +135,13 @@ struct LayerParams {
   // dependency met, 15 epilogue starts the phase's units.  Last row: kernel
   // start, inputs ready, kernel end, router top-k start and release.
   uint64_t* ts;
+  // per KV-head group dataflow QKV -> attention -> merge -> o-proj:
+  // [0..2][kMaxGroups] counters (finished QKV tiles, attention chunks, merge
+  // items; the last arrival resets it), [3..5][kMaxGroups] ready flags (epoch + 1)
+  uint32_t* grp_sync;
+  uint8_t qkv_order[64];           // QKV tile taken in claim position i (< 64): group by group
+  uint8_t grp_tiles[kMaxGroups];   // QKV tiles holding rows of group g
+  float* part_o;            // split-K partials of the o-proj (it overlaps the QKV phase)
 };
 constexpr int kTsSlots = 16;
 constexpr int kTsPerCta = (PH_COUNT + 1) * kTsSlots;
