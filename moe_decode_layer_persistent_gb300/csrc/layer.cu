@@ -1393,13 +1393,9 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
       // of its SwiGLU rows and releases them to the down units
       epi_sync();
       if (et == 0) {
-        __threadfence();
-        const uint32_t old = atomicAdd(P.exp_sync + e, 1u);
+        const uint32_t old = atom_add_acq_rel(P.exp_sync + e, 1u);
         const bool last = old == static_cast<uint32_t>(P.I / 128 - 1);
-        if (last) {
-          P.exp_sync[e] = 0;
-          __threadfence();
-        }
+        if (last) P.exp_sync[e] = 0;  // this launch's arrivals are all in
         m->flag = last;
       }
       epi_sync();
@@ -1444,13 +1440,9 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
     epi_sync();
     if (et == 0) {
       uint32_t* c = P.fix_ctr + ph * 256 + U.col_tile;
-      __threadfence();
-      const uint32_t old = atomicAdd(c, 1u);
+      const uint32_t old = atom_add_acq_rel(c, 1u);
       const bool last = old == static_cast<uint32_t>(U.ksplit - 1);
-      if (last) {
-        *c = 0;
-        __threadfence();
-      }
+      if (last) *c = 0;  // this launch's arrivals are all in
       m->flag = last;
     }
     epi_sync();
@@ -1501,13 +1493,9 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
     // the last finished router tile computes the top-k for every token
     epi_sync();
     if (et == 0) {
-      __threadfence();
-      const uint32_t old = atomicAdd(P.misc_ctr, 1u);
+      const uint32_t old = atom_add_acq_rel(P.misc_ctr, 1u);
       const bool last = old == static_cast<uint32_t>(P.tiles_router - 1);
-      if (last) {
-        *P.misc_ctr = 0;
-        __threadfence();
-      }
+      if (last) *P.misc_ctr = 0;  // this launch's arrivals are all in
       m->flag = last;
     }
     epi_sync();

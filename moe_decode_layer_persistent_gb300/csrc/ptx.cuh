@@ -290,6 +290,9 @@ MK_DEV uint32_t ld_acquire(const uint32_t* p) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+// Atomic add that releases this thread's (and, through a preceding barrier,
+// its group's) earlier writes and acquires the other arrivers' (one round
+// trip instead of a fence followed by an atomic).
 MK_DEV uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
   uint32_t old;
   asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
