@@ -222,12 +222,12 @@ MK_DEV uint32_t* grp_ctr(const LayerParams& P, int kind, int g) { return P.grp_s
 MK_DEV uint32_t* grp_flag(const LayerParams& P, int kind, int g) {
   return P.grp_sync + (3 + kind) * kMaxGroups + g;
 }
-// One thread, after the data it counts is written and fenced.
+// One thread, after the data it counts is written (by it, or by its group
+// before a barrier): the arrival releases it.
 MK_DEV void grp_count_in(const LayerParams& P, int kind, int g, uint32_t need, uint32_t epoch) {
   uint32_t* c = grp_ctr(P, kind, g);
-  if (atomicAdd(c, 1u) == need - 1u) {
+  if (atom_add_acq_rel(c, 1u) == need - 1u) {
     *c = 0;
-    __threadfence();
     st_release(grp_flag(P, kind, g), epoch + 1u);
   }
 }
@@ -1407,10 +1407,7 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
           P.srow_a[s] = a > 0.f ? __fdiv_rn(a, 2688.0f) : 1.0f;
         }
         epi_sync();
-        if (et == 0) {
-          __threadfence();
-          st_release(P.exp_sync + kMaxE + e, m->epoch + 1u);
-        }
+        if (et == 0) st_release(P.exp_sync + kMaxE + e, m->epoch + 1u);
       }
     } else {
       const float td = P.ts_down[e];
@@ -1484,7 +1481,6 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
     // this tile's q, k and v rows are final: count it in for its groups
     epi_sync();
     if (et == 0) {
-      __threadfence();
       for (int gg = 0; gg < P.Hkv; ++gg)
         if (tile_in_group(P, U.tile, gg)) grp_count_in(P, 0, gg, P.grp_tiles[gg], m->epoch);
     }
@@ -1506,7 +1502,6 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
       epi_sync();
       if (et == 0) stamp(P, S, PH_COUNT, 7);
       if (et == 0) {
-        __threadfence();
         red_release_add(P.bar_ctr + BAR_ROUTE, static_cast<uint32_t>(P.grid));
         stamp(P, S, PH_COUNT, 4);
       }
@@ -1774,18 +1769,16 @@ MK_DEV void combine_phase_end(const LayerParams& P, const Smem& S, int et) {
   Misc* m = S.m;
   const int tiles = P.P / 128;
   if (et == 0) m->n_done = 0;
-  epi_sync();
-  if (et == 0) __threadfence();
-  epi_sync();
+  epi_sync();  // every thread's z writes precede the arrivals below
   for (int i = et; i < P.T * tiles; i += 128) {
     const int t = i / tiles, j = i % tiles;
     const uint32_t c = m->comb_local[t][j];
     if (c == 0) continue;
     uint32_t* ctr = P.comb_ctr + t * tiles + j;
-    const uint32_t old = atomicAdd(ctr, c);
+    // releases this CTA's z rows, acquires the other contributors'
+    const uint32_t old = atom_add_acq_rel(ctr, c);
     if (old + c == static_cast<uint32_t>(P.topk)) {
       *ctr = 0;
-      __threadfence();
       m->done_pairs[atomicAdd(&m->n_done, 1)] = i;
     }
   }
@@ -1834,10 +1827,7 @@ MK_DEV void combine_phase_end(const LayerParams& P, const Smem& S, int et) {
 
 MK_DEV bool epi_arrive(const LayerParams& P, const Smem& S, int id, int et) {
   epi_sync();
-  if (et == 0) {
-    __threadfence();
-    red_release_add(P.bar_ctr + id, 1u);
-  }
+  if (et == 0) red_release_add(P.bar_ctr + id, 1u);  // releases the group's writes
   return true;
 }
 
@@ -1871,10 +1861,7 @@ MK_DEV void run_epilogue(const LayerParams& P, const Smem& S, uint32_t epoch) {
         if (P.d == 128) attention_unit<128>(P, S, g, lo, hi, c, et);
         else attention_unit<64>(P, S, g, lo, hi, c, et);
         epi_sync();
-        if (et == 0) {
-          __threadfence();
-          grp_count_in(P, 1, g, P.attn_chunks, epoch);
-        }
+        if (et == 0) grp_count_in(P, 1, g, P.attn_chunks, epoch);
       }
       if (!ok) break;
       if (et == 0) {
@@ -1900,10 +1887,7 @@ MK_DEV void run_epilogue(const LayerParams& P, const Smem& S, uint32_t epoch) {
         if (P.d == 128) merge_item<128>(P, u);
         else merge_item<64>(P, u);
         __syncwarp();
-        if (lane_id() == 0) {
-          __threadfence();
-          grp_count_in(P, 2, g, static_cast<uint32_t>(P.T * 4), epoch);
-        }
+        if (lane_id() == 0) grp_count_in(P, 2, g, static_cast<uint32_t>(P.T * 4), epoch);
       }
       // the epilogue warps agree on the outcome before their next barrier
       if (lane_id() == 0) m->red[0][w] = wok ? 1.f : 0.f;
