@@ -120,11 +120,24 @@ def expert_prefetch_line(a, b):
 
 
 # ------------------------------------------------------------------ ncu traffic
-def kernel_source_hash():
+def _code_only(text):
+    """C++ source without comments and whitespace (string literals kept)."""
+    import re
+    pat = re.compile(r'//[^\n]*|/\*.*?\*/|"(?:\\.|[^"\\])*"', re.S)
+    text = pat.sub(lambda m: m.group(0) if m.group(0).startswith('"') else " ", text)
+    return "".join(text.split())
+
+
+def kernel_source_hash(files=None):
+    """Hash of the kernel sources' code (comments and layout do not count)."""
     import glob
     import hashlib
-    files = sorted(glob.glob(os.path.join(ROOT, "moe_decode_layer_persistent_gb300", "csrc", "*")))
-    return hashlib.sha256(b"".join(open(f, "rb").read() for f in files)).hexdigest()[:16]
+    if files is None:
+        files = sorted(glob.glob(os.path.join(ROOT, "moe_decode_layer_persistent_gb300", "csrc", "*")))
+    h = hashlib.sha256()
+    for f in files:
+        h.update(_code_only(open(f, encoding="utf-8").read()).encode())
+    return h.hexdigest()[:16]
 
 
 def profiled_traffic(workload):

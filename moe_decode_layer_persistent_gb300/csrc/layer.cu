@@ -282,8 +282,8 @@ MK_DEV bool queue_pop_group(const LayerParams& P, const Smem& S, QCursor& q, int
   q.advance();
   return ok;
 }
-constexpr int kBarEpi = 1;     // warps 4-7
-constexpr int kBarStage = 2;   // warps 2-3
+constexpr int kBarEpi = 1;     // epilogue warps 8-11
+constexpr int kBarStage = 2;   // stager warps 5-6
 MK_DEV void epi_sync() { named_bar(kBarEpi, 128); }
 MK_DEV void stage_sync() { named_bar(kBarStage, 64); }
 
@@ -327,8 +327,10 @@ MK_DEV int phase_units(const LayerParams& P, const Smem& S, int ph) {
   return 0;
 }
 
-// First unit of this CTA in a phase (units are dealt round-robin, rotated by
-// phase so that the CTAs holding a phase's extra units change).
+// First unit of this CTA in a statically dealt phase (attention chunks, merge
+// items, and the first unit of the launch's first weight phase): units are
+// dealt round-robin, rotated by phase so that the CTAs holding a phase's
+// extra units change.
 MK_DEV int first_unit(const LayerParams& P, int ph) {
   const int rot = (ph * 37) % P.grid;
   return (static_cast<int>(blockIdx.x) + P.grid - rot) % P.grid;
@@ -811,7 +813,7 @@ MK_DEV void run_mma(const LayerParams& P, const Smem& S) {
   }
 }
 
-// ============================================================ stagers (warps 2-3)
+// ============================================================ stagers (warps 5-6)
 // Token operand of a bf16 unit.  The stager leader bulk-copies rows t < T of
 // src[t][k0 .. k0 + 64*nkb) (and the gain slice) into the landing area of the
 // operand buffer (issue_bf16, possibly one unit ahead); then all stager
@@ -1510,7 +1512,7 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
   return true;
 }
 
-// ------------------------------------------------------------ attention (warps 4-7)
+// ------------------------------------------------------------ attention (epilogue warps 8-11)
 MK_DEV void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "

@@ -32,9 +32,10 @@ enum PhaseId : int {
   PH_COUNT = 9
 };
 
-// Grid dependency counters (one per dependency stop).  Each CTA arrives once
-// per launch on every counter its layer uses; a launch waits for
-// (epoch + 1) * grid arrivals.
+// Grid dependency counters.  Each CTA arrives once per launch on every
+// counter its layer uses; a waiter waits for (epoch + 1) * grid arrivals.
+// QKV, ATTN, MERGE and GU only mark completion: the stages after them wait per
+// head group (grp_sync) or per expert (exp_sync) instead.
 enum BarrierId : int {
   BAR_QKV = 0,    // q and the new K/V rows written
   BAR_ATTN = 1,   // attention partials written
