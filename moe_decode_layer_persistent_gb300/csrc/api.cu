@@ -169,7 +169,8 @@ mk_status fill_step(const mk_layer* L, const mk_step_io* io, LayerParams& P) {
   const mk_layer_config& c = L->cfg;
   if (!io) return MK_ERR_INVALID_ARG;
   if (io->n_tokens < 1 || io->n_tokens > c.max_tokens) return MK_ERR_INVALID_ARG;
-  if (io->ctx_len < 0 || io->ctx_len + io->n_tokens > c.max_ctx) return MK_ERR_INVALID_ARG;
+  if (io->ctx_len < 0 || static_cast<int64_t>(io->ctx_len) + io->n_tokens > c.max_ctx)
+    return MK_ERR_INVALID_ARG;
   if (!io->x_in || !io->x_out || !io->k_cache || !io->v_cache) return MK_ERR_INVALID_ARG;
   if (io->x_in == io->x_out) return MK_ERR_INVALID_ARG;
   if (!(c.flags & MK_FIRST_LAYER) && !io->q_in) return MK_ERR_INVALID_ARG;
@@ -179,6 +180,8 @@ mk_status fill_step(const mk_layer* L, const mk_step_io* io, LayerParams& P) {
                         io->next_k_cache, io->next_v_cache, io->q_out};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return MK_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(io->topk_idx_out) | reinterpret_cast<uintptr_t>(io->topk_w_out)) & 3u)
+    return MK_ERR_INVALID_ARG;
   P = L->tmpl;
   P.T = io->n_tokens;
   P.ctx = io->ctx_len;
@@ -495,6 +498,7 @@ mk_status mk_stack_create(mk_layer* const* layers, int32_t n, mk_stack** out) {
 
 mk_status mk_stack_step(mk_stack* S, const mk_stack_io* io, void* stream) {
   if (!S || !io || !io->k_caches || !io->v_caches) return MK_ERR_INVALID_ARG;
+  if (io->n_tokens < 1 || io->n_tokens > kMaxT) return MK_ERR_INVALID_ARG;  // before offsets use it
   const int n = static_cast<int>(S->layers.size());
   std::vector<LayerParams> params(n);
   for (int l = 0; l < n; ++l) {

@@ -155,6 +155,33 @@ def test_expert_prefetch_statistics(cuda_lib):
     assert st["hits"] >= len(_predicted(idxs[0], N, E))  # step 2 repeats step 1's routing
 
 
+def test_step_rejects_bad_arguments_before_launch(cuda_lib):
+    """Malformed steps are refused on the host (MK_ERR_INVALID_ARG) before
+    anything is launched: a context whose end overflows, misaligned top-k
+    outputs, token counts outside 1..max_tokens, output aliasing input."""
+    work, _ = H.prepare("tiny_layer", "host", T=4, ctx=30, enforce=False)
+    c = work["cfgs"][0]
+    kc, vc = (t.clone() for t in work["caches"][0])
+    layer = H.make_layer(cuda_lib, c, work["Ws"][0], cuda_lib.MK_FIRST_LAYER, kc.shape[0])
+    x = work["x_in"][:4].contiguous()
+    y = torch.zeros_like(x)
+    idx = torch.zeros((4, c["top_k"] + 1), dtype=torch.int32, device="cuda")
+    bad = [cuda_lib.make_step_io(4, 2**31 - 1, x, y, kc, vc),
+           cuda_lib.make_step_io(4, 30, x, y, kc, vc, topk_idx_out=idx.data_ptr() + 2),
+           cuda_lib.make_step_io(0, 30, x, y, kc, vc),
+           cuda_lib.make_step_io(17, 30, x, y, kc, vc),
+           cuda_lib.make_step_io(4, 30, x, x, kc, vc)]
+    try:
+        for io in bad:
+            with pytest.raises(cuda_lib.MkError) as e:
+                cuda_lib.mk_decode_step(layer, io)
+            assert e.value.status == 1
+        torch.cuda.synchronize()
+        assert cuda_lib.mk_layer_status(layer) == 0
+    finally:
+        cuda_lib.mk_layer_destroy(layer)
+
+
 def test_bounded_wait_reports_timeout_and_recovers(cuda_lib):
     """A wait limit of 1 ns makes the first wait that is not already satisfied
     give up: the kernel returns, the status reads MK_ERR_TIMEOUT, the context
