@@ -255,7 +255,8 @@ mk_status mk_get_timestamps(mk_layer* layer, uint64_t* host_buf, size_t n);
  * with 16 small experts fit; the 4096-hidden, 256-expert shapes do not) are
  * rejected with MK_ERR_UNSUPPORTED before anything is launched (with
  * MK_LOG=1 a line on stderr says why); the attention split uses at most 32
- * chunks per KV head.
+ * chunks per KV head.  cfg->prefetch_experts is ignored: the shared array
+ * keeps no routing history from one call to the next.
  *
  * The first call on a device performs a one-time set-up with that device
  * current (it looks up the array's device address); make that first call
