@@ -243,14 +243,16 @@ class Runner:
         return self.B.mk_stack_status(self.stack) if self.stack is not None else \
             self.B.mk_layer_status(self.layers[0])
 
-    def drift(self, gen):
-        """Next step's input of a MoE workload: x <- 0.9 x + sqrt(0.19) n,
-        n ~ N(0, 1), so that consecutive steps route partly alike (the
-        previous step's most-used experts are the prefetch's prediction)."""
-        if not self.moe:
+    def drift(self, gen, mode="drift"):
+        """Next step's input of a MoE workload.  drift: x <- 0.9 x + sqrt(0.19) n,
+        n ~ N(0, 1), so that consecutive steps route partly alike (the previous
+        step's most-used experts are the prefetch's prediction); independent:
+        x <- n; fixed: unchanged."""
+        if not self.moe or mode == "fixed":
             return
         n = torch.randn(self.x_in.shape, generator=gen, device="cuda", dtype=torch.float32)
-        self.x_in.copy_((0.9 * self.x_in.float() + 0.19 ** 0.5 * n).to(torch.bfloat16))
+        a = 0.9 if mode == "drift" else 0.0
+        self.x_in.copy_((a * self.x_in.float() + (1.0 - a * a) ** 0.5 * n).to(torch.bfloat16))
 
     def experts_touched(self, hist=None):
         """Distinct experts per layer, averaged over the recorded steps."""
@@ -318,6 +320,9 @@ def main():
     ap.add_argument("--workload", default="swa_layer")
     ap.add_argument("--impl", default="mk", choices=["mk", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--inputs", default="drift", choices=["drift", "independent", "fixed"],
+                    help="MoE inputs between steps: x <- 0.9x + 0.436n (drift), a fresh "
+                         "draw (independent) or the same x (fixed)")
     ap.add_argument("--prefetch-experts", type=int, default=None,
                     help="MoE: experts of the previous step prefetched into L2 (default 0: "
                          "off, measured faster on these inputs)")
@@ -349,7 +354,7 @@ def main():
     hist = torch.zeros((args.steps,) + tuple(R.idx.shape), dtype=torch.int32, device="cuda")
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
-            R.drift(gen)
+            R.drift(gen, args.inputs)
             if flush is not None:
                 flush.fill_(1.0)
             R.step()
@@ -372,7 +377,7 @@ def main():
     t_wall0 = time.perf_counter()
     with torch.cuda.stream(stream):
         for i in range(args.steps):
-            R.drift(gen)
+            R.drift(gen, args.inputs)
             if flush is not None:
                 flush.fill_(float(i))
             evs[i][0].record(stream)
@@ -438,7 +443,9 @@ def main():
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "us_per_layer": round(us_step / R.L, 3),
         "experts_touched_mean": round(float(np.mean(touched)), 2) if R.moe else None,
-        "inputs": ("x_{s+1} = 0.9 x_s + 0.436 n_s per step (consecutive steps route partly alike)"
+        "inputs": ({"drift": "x_{s+1} = 0.9 x_s + 0.436 n_s per step (consecutive steps route partly alike)",
+                    "independent": "a fresh x_in per step",
+                    "fixed": "the same x_in every step"}[args.inputs]
                    if R.moe else "the same x_in every step"),
         "expert_prefetch": expert_prefetch_line(pf0, pf1) if R.moe else None,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
