@@ -237,6 +237,37 @@ def test_combine_is_weighted_sum_in_rank_order():
         assert np.array_equal(r["y"][t], n.bf16_round(acc))
 
 
+def test_combine_pairs_each_weight_with_its_expert():
+    """Experts identical except for a power-of-two down tensor scale 2^e, so
+    that every z of token t is 2^e times one vector z0_t (exactly: scaling by a
+    power of two commutes with every rounding).  Then y_t must be
+    bf16(sum_r w_tr 2^idx_tr z0_t) summed in rank order; a combine that pairs a
+    weight with another rank's expert, reorders the weights or renormalises
+    them gives another value on these inputs (checked)."""
+    rng = np.random.default_rng(22)
+    E, H, P, I, T, k = 5, 32, 32, 16, 3, 3
+    W = _moe_weights(rng, E, H, P, I)
+    for key in ("gate", "up", "down"):
+        for part in ("q", "s", "ts"):
+            arr = W["exp_%s_%s" % (key, part)]
+            arr[:] = arr[0]
+    h = bf(rng, T, H)
+    idx = np.array([[0, 3, 1], [4, 2, 0], [2, 1, 3]])
+    w = np.float32([[0.5, 0.25, 0.125], [0.375, 0.3125, 0.0625], [0.6, 0.2, 0.15]])
+    z0 = ol.moe_ffn(h, W, idx, w)["z"][:, 0]          # all experts alike: z of any rank
+    W["exp_down_ts"] = W["exp_down_ts"][0] * np.float32([2.0 ** e for e in range(E)])
+    r = ol.moe_ffn(h, W, idx, w)
+    for t in range(T):
+        want = np.zeros(P)
+        for j in range(k):
+            want = want + float(w[t, j]) * (2.0 ** idx[t, j]) * z0[t]
+        assert np.array_equal(r["y"][t], n.bf16_round(want)), t
+        # the inputs tell the correct pairing from a rotated one and from renormalised weights
+        rot = sum(float(w[t, (j + 1) % k]) * (2.0 ** idx[t, j]) * z0[t] for j in range(k))
+        assert not np.array_equal(n.bf16_round(want), n.bf16_round(rot))
+        assert not np.array_equal(n.bf16_round(want), n.bf16_round(want / float(w[t].sum())))
+
+
 # ------------------------------------------------------------ whole layer ---
 
 def _tiny_layer_inputs(rng, ffn="moe"):
@@ -274,7 +305,7 @@ def _torch_layer(cfg, W, x, kc, vc, ctx):
     h = r16(F.rms_norm(x_mid, (H,), t(W["ffn_norm_w"]), eps=1e-6))
     if cfg["ffn"] == "dense":
         a = r16(F.silu(F.linear(h, t(W["w_gate"]))) * F.linear(h, t(W["w_up"])))
-        return r16(x_mid + F.linear(a, t(W["w_down"]))).numpy(), None
+        return r16(x_mid + r16(F.linear(a, t(W["w_down"])))).numpy(), None
     logits = F.linear(h, t(W["w_router"])).float()
     top = torch.topk(logits, cfg["top_k"], dim=1)
     probs = torch.softmax(logits.double(), dim=1)
