@@ -8,7 +8,6 @@
 #include <new>
 #include <vector>
 
-#include "../../include/mk_selftest.h"
 #include "host_util.h"
 #include "layer.h"
 
@@ -370,6 +369,10 @@ mk_status mk_layer_create(const mk_layer_config* cfg, const mk_layer_weights* w,
     MK_TRY(dalloc(L, &P.comb_ctr, T * (P.P / 128)));
     MK_TRY(dalloc(L, &P.exp_sync, 2 * kMaxE));
     MK_TRY(dalloc(L, &P.srow_a, T * kMaxK));
+    // operand images: zero-filled here, so that inputs past K in the last
+    // K-block read as zero codes and zero scales in every later step
+    MK_TRY(dalloc(L, &P.pq_img, image_bytes(P.P)));
+    MK_TRY(dalloc(L, &P.aq_img, static_cast<size_t>(P.E) * image_bytes(P.I)));
     MK_TRY(dalloc(L, &P.pf_list, 2 * kMaxPf));
     MK_CUDA_TRY(cudaMemset(P.pf_list, 0xFF, 2 * kMaxPf * sizeof(int32_t)));  // empty lists
     MK_TRY(dalloc(L, &P.pf_stats, 4));
@@ -579,30 +582,6 @@ mk_status mk_get_timestamps(mk_layer* layer, uint64_t* host_buf, size_t n) {
   return MK_OK;
 }
 
-mk_status mk_selftest_copy_scratch(mk_layer* layer, int32_t which, void* dst, size_t bytes) {
-  if (!layer || !dst) return MK_ERR_INVALID_ARG;
-  const LayerParams& P = layer->tmpl;
-  const size_t T = kMaxT;
-  const void* src = nullptr;
-  size_t cap = 0;
-  switch (which) {
-    case 0: src = P.q_buf; cap = T * P.Hq * P.d * 2; break;
-    case 1: src = P.o_buf; cap = T * P.Hq * P.d * 2; break;
-    case 2: src = P.xmid; cap = T * P.H * 2; break;
-    case 3: src = P.logits; cap = T * kMaxE * 4; break;
-    case 4: src = P.p_buf; cap = T * P.P * 2; break;
-    case 5: src = P.a_buf; cap = P.moe ? T * P.topk * P.I * 2 : T * P.F * 2; break;
-    case 6: src = P.z_buf; cap = T * P.topk * P.P * 2; break;
-    case 7: src = P.y_buf; cap = T * P.P * 2; break;
-    case 8: src = P.idx; cap = T * kMaxK * 4; break;
-    case 9: src = P.wts; cap = T * kMaxK * 4; break;
-    default: return MK_ERR_INVALID_ARG;
-  }
-  if (!src || bytes > cap) return MK_ERR_INVALID_ARG;
-  MK_CUDA_TRY(cudaMemcpy(dst, src, bytes, cudaMemcpyDeviceToDevice));
-  return MK_OK;
-}
-
 void mk_stack_destroy(mk_stack* S) {
   if (!S) return;
   for (int i = 0; i < 2; ++i) {
@@ -675,10 +654,17 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_layer_config* cfg, const mk
       cudaDeviceProp prop;
       MK_CUDA_TRY(cudaGetDeviceProperties(&prop, dev));
       if (prop.major != 10 || prop.minor != 3) return MK_ERR_UNSUPPORTED;
+      // the same launch checks as mk_layer_create: the kernel's shared memory
+      // fits and one CTA per SM can be resident
+      if (layer_smem_bytes() > prop.sharedMemPerBlockOptin) return MK_ERR_UNSUPPORTED;
       void* p = nullptr;
       MK_CUDA_TRY(cudaGetSymbolAddress(&p, g_noalloc_scratch));
       MK_CUDA_TRY(cudaFuncSetAttribute(layer_kernel_ptr(), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        layer_smem_bytes()));
+      int per_sm = 0;
+      MK_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, layer_kernel_ptr(), kThreads,
+                                                                layer_smem_bytes()));
+      if (per_sm < 1) return MK_ERR_UNSUPPORTED;
       D.base = static_cast<uint8_t*>(p);
       D.sm_count = prop.multiProcessorCount;
       D.ready = true;
@@ -791,6 +777,8 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_layer_config* cfg, const mk
     P.comb_ctr = cv.take<uint32_t>(T * (P.P / 128));
     P.exp_sync = cv.take<uint32_t>(2 * kMaxE);
     P.srow_a = cv.take<float>(T * kMaxK);
+    P.pq_img = cv.take<uint8_t>(image_bytes(P.P));
+    P.aq_img = cv.take<uint8_t>(static_cast<size_t>(P.E) * image_bytes(P.I));
     part = std::max(part, static_cast<size_t>(P.ks_rp) * T * (P.tiles_router + P.tiles_pool) * 128);
     part = std::max(part, static_cast<size_t>(P.ks_unpool) * T * P.tiles_unpool * 128);
     gu = sf_repacked_bytes(P.E, P.I, P.P);
@@ -838,6 +826,10 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_layer_config* cfg, const mk
   if (P.comb_ctr) MK_CUDA_TRY(cudaMemsetAsync(P.comb_ctr, 0, T * (P.P / 128) * 4, s));
   if (P.exp_sync) MK_CUDA_TRY(cudaMemsetAsync(P.exp_sync, 0, 2 * kMaxE * 4, s));
   if (P.moe) {
+    // the operand images' padding past K must read as zero (an earlier call
+    // may have left other shapes' data in the array)
+    MK_CUDA_TRY(cudaMemsetAsync(P.pq_img, 0, image_bytes(P.P), s));
+    MK_CUDA_TRY(cudaMemsetAsync(P.aq_img, 0, static_cast<size_t>(P.E) * image_bytes(P.I), s));
     st = launch_sf_repack(w->exp_gate_s, const_cast<uint8_t*>(P.sf_gate), P.E, P.I, P.P, s);
     if (st == MK_OK) st = launch_sf_repack(w->exp_up_s, const_cast<uint8_t*>(P.sf_up), P.E, P.I, P.P, s);
     if (st == MK_OK) st = launch_sf_repack(w->exp_down_s, const_cast<uint8_t*>(P.sf_down), P.E, P.P, P.I, s);

@@ -44,7 +44,6 @@ constexpr uint32_t kOffB = kOffSF + kStages * kSfBytes;       // 2 operand buffe
 constexpr uint32_t kBBufBytes = 40960;
 constexpr uint32_t kBSfOff = 16384;                          // scales inside a B buffer
 constexpr uint32_t kLandOff = 16384;   // bf16 units: raw input rows (<= 16 KB), then the gain slice
-constexpr uint32_t kFp4LandOff = 32768; // NVFP4 units: two 4 KB row slots, one per stager warp
 constexpr uint32_t kOffMisc = kOffB + 2 * kBBufBytes;
 constexpr uint32_t kOffTs = kOffMisc + 8192;                 // self-timing block
 constexpr uint32_t kSmemBytes = kOffTs + kTsPerCta * 8 + 1024;   // + alignment slack
@@ -58,7 +57,7 @@ struct Misc {
   uint64_t accempty[2];
   uint64_t route_ready;
   uint64_t mma_done;
-  uint64_t land[2][3];             // stager landing copies per operand buffer: [0] bf16 rows, [1..2] per-warp rows
+  uint64_t land[2];                // stager copies into each operand buffer (bf16 input rows or an NVFP4 image)
   uint64_t attn_free;              // the epilogue's attention no longer uses the operand buffers
   uint64_t uq_full[8];             // unit queue: slot written by the producer
   uint64_t uq_empty[8];            // unit queue: slot read by the 4 MMA issuers, stager and epilogue leaders
@@ -72,8 +71,9 @@ struct Misc {
   int off[kMaxE + 1];              // first slot of expert e in `slots`
   int slots[kMaxT * kMaxK];        // slot (t*k + r) grouped by expert
   float rnorm[kMaxT];              // stager: RMSNorm factors of the phase input
-  float srow_st[kMaxT * kMaxK];    // stager: NVFP4 row scales of the phase input
+  float srow_st[kMaxT];            // stager: row scales of p (its share of the p image)
   float srow_ep[kMaxT * kMaxK];    // epilogue: NVFP4 row scales of the phase input
+  float srow_q[kMaxT];             // epilogue: row scales of the rows it quantises into an image
   float red[4][kMaxT];             // epilogue cross-warp reductions
   uint32_t comb_local[kMaxT][16];  // epilogue: this CTA's z contributions per (token, tile)
   int done_pairs[kMaxT * 16];      // epilogue: (token, tile) pairs this CTA completes
@@ -81,7 +81,7 @@ struct Misc {
   int grp_ok[4];                   // shared outcome of a group's wait: [0] stagers, [1] epilogue, [2..3] stager warps
   int pref_ok[2];                  // stagers: a unit's first input rows were copied ahead (per buffer)
   int uq[8];                       // unit queue: the CTA's next units in order, -1 ends a phase
-  uint32_t land_out[2][3];         // landing copies issued and not yet consumed (per buffer, slot)
+  uint32_t land_out[2];            // stager copies issued and not yet waited for (per buffer)
 };
 static_assert(sizeof(Misc) <= 8192, "misc region");
 
@@ -341,7 +341,7 @@ MK_DEV int phase_dep(const LayerParams& P, int ph) {
   switch (ph) {
     case PH_O: return -1;  // per group of merged heads (grp_sync)
     case PH_RP: return BAR_O;
-    case PH_GU: return BAR_RP;
+    case PH_GU: return -1;                     // the p image (misc_ctr[2])
     case PH_DOWN: return P.moe ? -1 : BAR_RP;  // MoE: per expert (exp_sync)
     case PH_UNPOOL: return BAR_DOWN;
     case PH_NQKV: return BAR_X;
@@ -841,8 +841,8 @@ MK_DEV void issue_bf16(const LayerParams& P, const Smem& S, int ph, const Unit& 
   uint8_t* graw = raw + kMaxT * U.nkb * 128;
   const uint32_t rowbytes = static_cast<uint32_t>(U.nkb) * 128u;
   const uint64_t pol = policy_evict_last();
-  uint64_t* lb = &S.m->land[buf][0];
-  S.m->land_out[buf][0] = 1;
+  uint64_t* lb = &S.m->land[buf];
+  S.m->land_out[buf] = 1;
   mbar_arrive_expect_tx(lb, P.T * rowbytes + (src.gain ? rowbytes : 0u));
   for (int t = 0; t < P.T; ++t)
     bulk_load(raw + t * rowbytes, src.src + static_cast<size_t>(t) * src.ld + U.x0, rowbytes, lb, pol);
@@ -859,10 +859,10 @@ MK_DEV bool stage_bf16(const LayerParams& P, const Smem& S, int ph, const Unit& 
   uint8_t* raw = bb + kLandOff;
   uint8_t* graw = raw + kMaxT * nkb * 128;
   const uint32_t rowbytes = static_cast<uint32_t>(nkb) * 128u;
-  if (!group_mbar_wait(P, S, &S.m->land[buf][0], land_ph, ERR_TIMEOUT_B, tid == 0, kBarStage, 64, 0))
+  if (!group_mbar_wait(P, S, &S.m->land[buf], land_ph, ERR_TIMEOUT_B, tid == 0, kBarStage, 64, 0))
     return false;
   land_ph ^= 1;
-  if (tid == 0) S.m->land_out[buf][0] = 0;
+  if (tid == 0) S.m->land_out[buf] = 0;
   const int chunks = nkb * 8;  // 16-byte chunks per row
   for (int i = tid; i < kMaxT * chunks; i += 64) {
     const int t = i / chunks, c = i % chunks;
@@ -889,99 +889,97 @@ MK_DEV bool stage_bf16(const LayerParams& P, const Smem& S, int ph, const Unit& 
   return true;
 }
 
-// Quantiser sink with a given row scale.
-template <class Sink>
-MK_DEV void quantize_row_given_srow(const __nv_bfloat16* row, int K, float s_row, Sink& sink) {
-  const int lane = lane_id();
-  const float d6 = __fmul_rn(6.0f, s_row);
-  for (int b = lane; b < (K >> 4); b += 32) {
+// NVFP4 row scale of p's row t (amax over the pooler tiles' partials).
+MK_DEV float p_row_scale(const LayerParams& P, int t) {
+  float a = 0.f;
+  for (int j = 0; j < P.P / 128; ++j) a = fmaxf(a, __ldcg(P.pamax + j * kMaxT + t));
+  return a > 0.f ? __fdiv_rn(a, 2688.0f) : 1.0f;
+}
+
+// This CTA's 1/grid share of the p image's 16-element blocks (T rows of P), by
+// the 64 stager threads: one block per thread at the full shapes.
+MK_DEV void p_image_share(const LayerParams& P, const Smem& S, int tid) {
+  Misc* m = S.m;
+  if (tid < P.T) m->srow_st[tid] = p_row_scale(P, tid);
+  stage_sync();
+  const int nblk = P.P / 16, total = P.T * nblk;
+  const int per = (total + P.grid - 1) / P.grid;
+  const int lo = static_cast<int>(blockIdx.x) * per, hi = min(total, lo + per);
+  OperandSink sink{P.pq_img, P.pq_img + ((P.P + 255) / 256) * 2048, 0};
+  for (int i = lo + tid; i < hi; i += 64) {
+    const int t = i / nblk, b = i % nblk;
     float x[16];
-    load_bf16x16(row + b * 16, x);
-    float a16 = 0.f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) a16 = fmaxf(a16, fabsf(x[i]));
-    const uint32_t sb = cvt_e4m3(__fdiv_rn(a16, d6));
-    const float sbf = e4m3_to_float(sb);
-    uint32_t w0 = 0, w1 = 0;
-    if (sbf > 0.f) {
-      e2m1_codes16(x, __fmul_rn(sbf, s_row), w0, w1);
-    }
+    load_bf16x16_cg(P.p_buf + static_cast<size_t>(t) * P.P + b * 16, x);
+    uint32_t w0, w1, sb;
+    quantize_block16(x, m->srow_st[t], w0, w1, sb);
+    sink.r = static_cast<uint32_t>(t);
     sink.put(b, w0, w1, sb);
   }
+  fence_proxy_async_global();  // read by every CTA's bulk copies
 }
 
-// Token operand of an NVFP4 expert unit: row i = the i-th slot routed to the
-// expert, quantised from its bf16 row (p for gate/up, the SwiGLU output for
-// down).  Stager warp w handles rows w, w+2, ...: each row is first
-// bulk-copied into the warp's landing slot of the operand buffer (the first
-// one by issue_fp4_row, possibly one unit ahead).
-MK_DEV const __nv_bfloat16* fp4_row(const LayerParams& P, const Smem& S, const Unit& U, bool gu, int i) {
-  const int s = S.m->slots[S.m->off[U.expert] + i];
-  return gu ? P.p_buf + static_cast<size_t>(s / P.topk) * P.P : P.a_buf + static_cast<size_t>(s) * P.I;
+// Token operand of an NVFP4 expert unit: an operand image quantised once per
+// launch (the p image for every gate/up unit, the expert's SwiGLU image for a
+// down unit), bulk-copied by the stager leader into operand buffer `buf`:
+// codes to the buffer's start, scale chunks to kBSfOff.
+MK_DEV void issue_image(const LayerParams& P, const Smem& S, const uint8_t* img, int K, int buf) {
+  const uint32_t half = image_bytes(K) / 2;
+  uint64_t* lb = &S.m->land[buf];
+  S.m->land_out[buf] = 1;
+  mbar_arrive_expect_tx(lb, 2 * half);
+  const uint64_t pol = policy_evict_last();
+  bulk_load(S.bbuf(buf), img, half, lb, pol);
+  bulk_load(S.bbuf(buf) + kBSfOff, img + half, half, lb, pol);
 }
 
-// Lane 0 of stager warp w: bulk-copy row i of unit U into the warp's slot.
-MK_DEV void issue_fp4_row(const LayerParams& P, const Smem& S, const Unit& U, bool gu, int i,
-                          int buf, int w) {
-  uint64_t* lb = &S.m->land[buf][1 + w];
-  const uint32_t rowbytes = static_cast<uint32_t>(U.K) * 2u;
-  S.m->land_out[buf][1 + w] = 1;
-  mbar_arrive_expect_tx(lb, rowbytes);
-  bulk_load(S.bbuf(buf) + kFp4LandOff + w * 4096, fp4_row(P, S, U, gu, i), rowbytes, lb,
-            policy_evict_last());
-}
-
-MK_DEV bool stage_fp4(const LayerParams& P, const Smem& S, const Unit& U, bool gu, int buf,
-                      bool first_issued, uint32_t (&land_ph)[2][3]) {
+// The stagers through one NVFP4 expert phase.  Each unit's operand is a copy
+// of an image, skipped when the buffer already holds that image (every gate/up
+// unit uses the p image; consecutive down units may share an expert).  A down
+// unit waits for its own expert's image only.
+MK_DEV bool stage_expert_phase(const LayerParams& P, const Smem& S, int ph, uint32_t epoch, QCursor& q,
+                               uint32_t (&b_ph)[2], uint32_t& ucount, uint32_t (&land_ph)[2]) {
   Misc* m = S.m;
-  const int warp = (threadIdx.x - kStagerBase) >> 5;  // 0..1
-  const int n = m->off[U.expert + 1] - m->off[U.expert];
-  const int K = U.K;
-  uint8_t* bb = S.bbuf(buf);
-  // K-block padding beyond K must read as zero codes and zero scales
-  if (K % 256) {
-    const int tid = threadIdx.x - kStagerBase;
-    const int kb = K / 256, pad_from = (K % 256) / 2;  // bytes of the last K-block row in use
-    for (int i = tid; i < kMaxT * 128; i += 64) {
-      const int r = i / 128, byte = i % 128;
-      if (byte >= pad_from) bb[kb * 2048 + sw128_offset(r, byte)] = 0;
+  const int tid = threadIdx.x - kStagerBase;
+  const bool gu = ph == PH_GU;
+  const int K = gu ? P.P : P.I;
+  int holds[2] = {-1, -1};  // image in each operand buffer: -2 the p image, e expert e's
+  if (gu && !group_grid_wait(P, S, BAR_PQ, grid_target(P, epoch), tid == 0, kBarStage, 64, 0)) return false;
+  if (tid == 0) stamp(P, S, ph, 14);
+  int u;
+  if (!queue_pop_group(P, S, q, u, tid == 0, kBarStage, 64, 0)) return false;
+  while (u >= 0) {
+    const Unit U = make_unit(P, S, ph, u);
+    const uint32_t b = ucount & 1;
+    const uint64_t w0 = tnow(P);
+    if (!gu && !group_flag_wait(P, S, P.exp_sync + kMaxE + U.expert, epoch + 1u, tid == 0, kBarStage, 64, 0))
+      return false;
+    if (!group_mbar_wait(P, S, &m->bempty[b], b_ph[b] ^ 1, ERR_TIMEOUT_B, tid == 0, kBarStage, 64, 0))
+      return false;
+    const uint64_t w1 = tnow(P);
+    const int key = gu ? -2 : U.expert;
+    if (holds[b] != key) {
+      if (tid == 0) {
+        fence_proxy_async_global();  // the image was written by ordinary stores of another CTA
+        issue_image(P, S, gu ? P.pq_img : P.aq_img + static_cast<size_t>(U.expert) * image_bytes(K), K, b);
+      }
+      if (!group_mbar_wait(P, S, &m->land[b], land_ph[b], ERR_TIMEOUT_B, tid == 0, kBarStage, 64, 0))
+        return false;
+      land_ph[b] ^= 1;
+      if (tid == 0) m->land_out[b] = 0;
+      holds[b] = key;
     }
-    for (int i = tid; i < 512 * (4 - (K % 256) / 64); i += 64)
-      bb[kBSfOff + (kb * 4 + (K % 256) / 64) * 512 + i] = 0;
-  }
-  uint8_t* slot = bb + kFp4LandOff + warp * 4096;
-  uint64_t* lb = &m->land[buf][1 + warp];
-  for (int i = warp; i < n; i += 2) {
-    if (i != warp || !first_issued) {
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane_id() == 0) issue_fp4_row(P, S, U, gu, i, buf, warp);
+    if (tid == 0) {
+      mbar_arrive(&m->bfull[b]);
+      if (P.ts) {
+        stamp_add(P, S, ph, 8, w1 - w0);
+        stamp_add(P, S, ph, 9, globaltimer() - w1);
+      }
     }
-    const int s = m->slots[m->off[U.expert] + i];
-    // gate/up rows: the token's scale (phase start); down rows: the scale the
-    // expert's last gate/up tile published, loaded while the row lands
-    const float srow = gu ? m->srow_st[s / P.topk] : __ldcg(P.srow_a + s);
-    int wok = 0;
-    if (lane_id() == 0) wok = wait_bar(P, S, lb, land_ph[buf][1 + warp], ERR_TIMEOUT_B) ? 1 : 0;
-    if (!__shfl_sync(0xffffffffu, wok, 0)) return false;
-    land_ph[buf][1 + warp] ^= 1;
-    if (lane_id() == 0) m->land_out[buf][1 + warp] = 0;
-    OperandSink sink{bb, bb + kBSfOff, static_cast<uint32_t>(i)};
-    quantize_row_given_srow(reinterpret_cast<const __nv_bfloat16*>(slot), K, srow, sink);
+    b_ph[b] ^= 1;
+    ++ucount;
+    if (!queue_pop_group(P, S, q, u, tid == 0, kBarStage, 64, 0)) return false;
   }
   return true;
-}
-
-// Prefetch of a unit's inputs into operand buffer `buf`'s landing area, by
-// the stager leader: the bf16 rows, or the first row of each stager warp's
-// slot for NVFP4 units.
-MK_DEV void prefetch_unit(const LayerParams& P, const Smem& S, int ph, const Unit& U, int buf) {
-  if (!U.fp4) {
-    issue_bf16(P, S, ph, U, buf);
-    return;
-  }
-  const int n = S.m->off[U.expert + 1] - S.m->off[U.expert];
-  for (int w = 0; w < 2 && w < n; ++w) issue_fp4_row(P, S, U, ph == PH_GU, w, buf, w);
 }
 
 // RMSNorm factors of x_in (first layer), by the stager and epilogue warps: one row per warp at a
@@ -1018,21 +1016,30 @@ MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
   const int tid = threadIdx.x - kStagerBase;  // 0..63
   const int warp = tid >> 5;
   const uint32_t target = grid_target(P, epoch);
-  uint32_t b_ph[2] = {0, 0}, ucount = 0, land_ph[2][3] = {{0, 0, 0}, {0, 0, 0}};
+  uint32_t b_ph[2] = {0, 0}, ucount = 0, land_ph[2] = {0, 0};
   QCursor q;
   bool ok = true;
   if (P.first_layer) rnorm_x_in(P, S);
   for (int ph = 0; ph < PH_COUNT && ok; ++ph) {
     if (!phase_is_gemm(ph) || !phase_active(P, ph)) continue;
     if (ph == PH_GU) {
+      // once p is complete, this CTA's share of the p image
+      if (!group_flag_wait(P, S, P.misc_ctr + 2, epoch + 1u, tid == 0, kBarStage, 64, 0)) { ok = false; break; }
+      p_image_share(P, S, tid);
+      stage_sync();
+      if (tid == 0) red_release_add(P.bar_ctr + BAR_PQ, 1u);
       // the expert weights depend only on the routing: publish it to the
-      // producer before waiting for the pooler output
+      // producer before waiting for the rest of the p image
       if (!group_grid_wait(P, S, BAR_ROUTE, target, tid == 0, kBarStage, 64, 0)) { ok = false; break; }
       if (warp == 0) {
         build_routing(P, S);
         __syncwarp();
         if (lane_id() == 0) mbar_arrive(&m->route_ready);
       }
+    }
+    if (ph == PH_GU || (ph == PH_DOWN && P.moe)) {
+      ok = stage_expert_phase(P, S, ph, epoch, q, b_ph, ucount, land_ph);
+      continue;
     }
     const int dep = phase_dep(P, ph);
     if (dep >= 0) {
@@ -1047,33 +1054,22 @@ MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
         for (int j = 0; j < P.H / 128; ++j) s += __ldcg(ssq + j * kMaxT + tid);
         m->rnorm[tid] = 1.0f / sqrtf(s / P.H + P.eps);
       }
-    } else if (ph == PH_GU) {
-      if (tid < P.T) {
-        float a = 0.f;
-        for (int j = 0; j < P.P / 128; ++j) a = fmaxf(a, __ldcg(P.pamax + j * kMaxT + tid));
-        m->srow_st[tid] = a > 0.f ? __fdiv_rn(a, 2688.0f) : 1.0f;
-      }
     }
     stage_sync();
-    // expert down units wait for their own expert's gate/up tiles, not for
-    // the whole phase: their rows are copied ahead only once it is ready
-    // units that wait for their own inputs instead of a whole phase: expert
-    // down (its expert's gate/up tiles), o-proj (its K-slice's head groups)
-    const bool per_unit = (ph == PH_DOWN && P.moe) || ph == PH_O;
+    // o-proj units wait for their own K-slice's head groups, not for the
+    // whole merge phase
+    const bool per_unit = ph == PH_O;
     auto unit_ready = [&](const Unit& V) -> bool {  // non-blocking (leader)
-      if (ph == PH_O) {
-        for (int g = o_group_lo(P, V); g <= o_group_hi(P, V); ++g)
-          if (!grp_ready(P, 2, g, epoch)) return false;
-        return true;
-      }
-      return static_cast<int32_t>(ld_acquire(P.exp_sync + kMaxE + V.expert) - (epoch + 1u)) >= 0;
+      for (int g = o_group_lo(P, V); g <= o_group_hi(P, V); ++g)
+        if (!grp_ready(P, 2, g, epoch)) return false;
+      return true;
     };
     // The leader copies a unit's first inputs ahead into the buffer's landing
     // area and records whether it did (read by all after the next barrier).
     auto try_prefetch = [&](const Unit& V, int buf) {
       if (tid != 0) return;
       const bool ready = !per_unit || unit_ready(V);
-      if (ready) prefetch_unit(P, S, ph, V, buf);
+      if (ready) issue_bf16(P, S, ph, V, buf);
       m->pref_ok[buf] = ready ? 1 : 0;
     };
     // attention keeps its tiles in the operand buffers: the o-proj (which no
@@ -1108,18 +1104,12 @@ MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
       const bool pre = *reinterpret_cast<volatile int*>(&m->pref_ok[b]) != 0;
       if (per_unit && !pre) {
         // not ready when looked at ahead: wait for the unit's inputs now
-        if (ph == PH_O) {
-          for (int g = o_group_lo(P, U); g <= o_group_hi(P, U) && ok; ++g)
-            ok = group_flag_wait(P, S, grp_flag(P, 2, g), epoch + 1u, tid == 0, kBarStage, 64, 0);
-        } else {
-          ok = group_flag_wait(P, S, P.exp_sync + kMaxE + U.expert, epoch + 1u, tid == 0, kBarStage, 64, 0);
-        }
+        for (int g = o_group_lo(P, U); g <= o_group_hi(P, U) && ok; ++g)
+          ok = group_flag_wait(P, S, grp_flag(P, 2, g), epoch + 1u, tid == 0, kBarStage, 64, 0);
         if (!ok) break;
       }
       const uint64_t w1 = tnow(P);
-      bool sok = true;
-      if (U.fp4) sok = stage_fp4(P, S, U, ph == PH_GU, b, pre, land_ph);
-      else sok = stage_bf16(P, S, ph, U, b, pre, land_ph[b][0]);
+      const bool sok = stage_bf16(P, S, ph, U, b, pre, land_ph[b]);
       // both stager warps agree on the outcome before the next barrier
       if (lane_id() == 0) m->grp_ok[2 + warp] = sok ? 1 : 0;
       fence_proxy_async_smem();
@@ -1140,14 +1130,13 @@ MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
       if (!queue_pop_group(P, S, q, u, tid == 0, kBarStage, 64, 0)) { ok = false; break; }
     }
   }
-  // landing copies still in flight (only after an abort) must land before exit
+  // copies still in flight (only after an abort) must land before exit
   stage_sync();
-  if (lane_id() == 0) {
-    for (int i = 0; i < 6; ++i) {
-      const int buf = i / 3, sl = i % 3;
-      if (!(sl == 0 ? tid == 0 : warp == sl - 1) || !m->land_out[buf][sl]) continue;
+  if (tid == 0) {
+    for (int buf = 0; buf < 2; ++buf) {
+      if (!m->land_out[buf]) continue;
       const uint64_t t0 = globaltimer();
-      while (!mbar_try_wait_sleep(&m->land[buf][sl], land_ph[buf][sl], 1000u)) {
+      while (!mbar_try_wait_sleep(&m->land[buf], land_ph[buf], 1000u)) {
         if (globaltimer() - t0 > P.timeout_ns) break;
       }
     }
@@ -1155,14 +1144,15 @@ MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
 }
 
 // ============================================================ epilogue (warps 8-11)
-// Cross-warp reduction over the 128 epilogue threads of 16 per-token values:
-// returns, in thread t (< 16), the sum (or max) for token t.
+// Cross-warp reduction over the 128 epilogue threads of 16 per-token values
+// (the tokens in `mask`): returns, in thread t (< 16, in mask), the sum (or
+// max) for token t.
 template <bool kMax>
-MK_DEV float epi_reduce16(const Smem& S, float (&v)[kMaxT], int et, int n) {
+MK_DEV float epi_reduce16_mask(const Smem& S, float (&v)[kMaxT], int et, uint32_t mask) {
   const int q = et >> 5;
 #pragma unroll
   for (int t = 0; t < kMaxT; ++t) {
-    if (t < n) {
+    if ((mask >> t) & 1u) {
       float x = v[t];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
@@ -1174,13 +1164,91 @@ MK_DEV float epi_reduce16(const Smem& S, float (&v)[kMaxT], int et, int n) {
   }
   epi_sync();
   float r = 0.f;
-  if (et < n) {
+  if (et < kMaxT && ((mask >> et) & 1u)) {
     r = S.m->red[0][et];
     for (int w = 1; w < 4; ++w) r = kMax ? fmaxf(r, S.m->red[w][et]) : r + S.m->red[w][et];
   }
   epi_sync();
   return r;
 }
+// The same over all 16 tokens (values of tokens >= T are 0): a butterfly
+// reduce-scatter inside each warp -- at each step a lane sends the half of
+// its values that its partner keeps, 8 + 4 + 2 + 1 + 1 shuffles instead of
+// 16 x 5 -- leaves token (lane >> 1) in lane pair (2t, 2t+1); then the four
+// warps through shared memory.  Thread t (< 16) gets token t's result.
+template <bool kMax>
+MK_DEV float epi_reduce16(const Smem& S, float (&v)[kMaxT], int et) {
+  const int lane = lane_id();
+  auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
+  float a8[8], a4[4], a2[2];
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    a8[i] = op(b4 ? v[i + 8] : v[i], __shfl_xor_sync(0xffffffffu, b4 ? v[i] : v[i + 8], 16));
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    a4[i] = op(b3 ? a8[i + 4] : a8[i], __shfl_xor_sync(0xffffffffu, b3 ? a8[i] : a8[i + 4], 8));
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+    a2[i] = op(b2 ? a4[i + 2] : a4[i], __shfl_xor_sync(0xffffffffu, b2 ? a4[i] : a4[i + 2], 4));
+  float a1 = op(b1 ? a2[1] : a2[0], __shfl_xor_sync(0xffffffffu, b1 ? a2[0] : a2[1], 2));
+  a1 = op(a1, __shfl_xor_sync(0xffffffffu, a1, 1));
+  if ((lane & 1) == 0) S.m->red[et >> 5][lane >> 1] = a1;
+  epi_sync();
+  float r = 0.f;
+  if (et < kMaxT) {
+    r = S.m->red[0][et];
+    for (int w = 1; w < 4; ++w) r = op(r, S.m->red[w][et]);
+  }
+  epi_sync();
+  return r;
+}
+
+// NVFP4 operand image (codes in K-blocks of 2048 B, then the scale chunks) of
+// `rows` bf16 rows of K inputs, by the 128 epilogue threads: image row i is
+// the row at src + off(i), with row scale srow[i] (shared memory).  Each
+// thread loads four 16-element blocks before quantising them, so that four
+// L2 round trips overlap.
+template <class Off>
+MK_DEV void quantize_image(uint8_t* img, int rows, int K, const float* srow,
+                           const __nv_bfloat16* src, Off off, int et) {
+  const int nblk = K / 16;
+  const int total = rows * nblk;
+  OperandSink sink{img, img + ((K + 255) / 256) * 2048, 0};
+  for (int i0 = et; i0 < total; i0 += 4 * 128) {
+    uint4 r[4][2];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int i = i0 + q * 128;
+      if (i < total) {
+        const uint4* p = reinterpret_cast<const uint4*>(src + off(i / nblk) + (i % nblk) * 16);
+        r[q][0] = __ldcg(p);
+        r[q][1] = __ldcg(p + 1);
+      }
+    }
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {
+      const int i = i0 + q * 128;
+      if (i >= total) break;
+      // select the block's registers (no dynamically indexed array)
+      const uint4 c0 = q == 0 ? r[0][0] : q == 1 ? r[1][0] : q == 2 ? r[2][0] : r[3][0];
+      const uint4 c1 = q == 0 ? r[0][1] : q == 1 ? r[1][1] : q == 2 ? r[2][1] : r[3][1];
+      const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+      float x[16];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        x[2 * k] = __uint_as_float(w[k] << 16);
+        x[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+      }
+      uint32_t w0, w1, sb;
+      quantize_block16(x, srow[i / nblk], w0, w1, sb);
+      sink.r = static_cast<uint32_t>(i / nblk);
+      sink.put(i % nblk, w0, w1, sb);
+    }
+  }
+  fence_proxy_async_global();  // read by other CTAs' bulk copies
+}
+
 
 // Router: top-k of the float32 logits (descending, an exact tie going to the
 // lower expert index), softmax over all experts, combine weights.  Warp w
@@ -1292,20 +1360,28 @@ MK_DEV void epi_bf16_final(const LayerParams& P, const Smem& S, int ph, const Un
     case PH_O:
     case PH_UNPOOL:
     case PH_DOWN: {  // residual: x = bf16(res + acc); sum-of-squares partial
+      // (the dense MLP's output is a bf16 activation itself: x = bf16(res + bf16(acc)))
       const __nv_bfloat16* res = ph == PH_O ? P.x_in : P.xmid;
       __nv_bfloat16* dst = ph == PH_O ? P.xmid : P.x_out;
+      const bool round_acc = ph == PH_DOWN;
+      // every residual load is issued before the first store: a load may not
+      // move past a store that could alias it, so interleaving them would cost
+      // one memory round trip per token
+      float rv[kMaxT];
+#pragma unroll
+      for (int t = 0; t < kMaxT; ++t)
+        rv[t] = (valid && t < P.T) ? ld_bf(res + static_cast<size_t>(t) * P.H + f) : 0.f;
       float sq[kMaxT];
 #pragma unroll
       for (int t = 0; t < kMaxT; ++t) {
         sq[t] = 0.f;
         if (valid && t < P.T) {
-          const size_t o = static_cast<size_t>(t) * P.H + f;
-          const float x = round_bf(ld_bf(res + o) + g[t]);
-          dst[o] = to_bf(x);
+          const float x = round_bf(rv[t] + (round_acc ? round_bf(g[t]) : g[t]));
+          dst[static_cast<size_t>(t) * P.H + f] = to_bf(x);
           sq[t] = x * x;
         }
       }
-      const float r = epi_reduce16<false>(S, sq, et, P.T);
+      const float r = epi_reduce16<false>(S, sq, et);
       if (et < P.T) (ph == PH_O ? P.ssq_mid : P.ssq_out)[U.tile * kMaxT + et] = r;
       break;
     }
@@ -1330,7 +1406,7 @@ MK_DEV void epi_bf16_final(const LayerParams& P, const Smem& S, int ph, const Un
             am[t] = fabsf(x);
           }
         }
-        const float r = epi_reduce16<true>(S, am, et, P.T);
+        const float r = epi_reduce16<true>(S, am, et);
         if (et < P.T) P.pamax[U.tile * kMaxT + et] = r;
       }
       break;
@@ -1375,24 +1451,38 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
     const int n = m->off[e + 1] - m->off[e];
     const int f = U.tile * 128 + et;
     if (ph == PH_GU) {
+      // Accumulator column t is token t (the p image holds every token).  The
+      // expert's slots, ascending, name its tokens in ascending order.
       const float tg = P.ts_gate[e], tu = P.ts_up[e];
+      const int* sl = m->slots + m->off[e];
       float am[kMaxT];
+      uint32_t tmask = 0;
+      int j = 0, sj = n > 0 ? sl[0] : 0;
+      int tj = n > 0 ? sj / P.topk : -1;
 #pragma unroll
-      for (int i = 0; i < kMaxT; ++i) {
-        am[i] = 0.f;
-        if (i < n) {
-          const int s = m->slots[m->off[e] + i];
-          const float sr = m->srow_ep[s / P.topk];
-          const float gv = g[i] * sr * tg, uv = u[i] * sr * tu;
+      for (int t = 0; t < kMaxT; ++t) {
+        am[t] = 0.f;
+        if (tj == t) {
+          const float sr = m->srow_ep[t];
+          const float gv = g[t] * sr * tg, uv = u[t] * sr * tu;
           const float a = round_bf(silu(gv) * uv);
-          P.a_buf[static_cast<size_t>(s) * P.I + f] = to_bf(a);
-          am[i] = fabsf(a);
+          P.a_buf[static_cast<size_t>(sj) * P.I + f] = to_bf(a);
+          am[t] = fabsf(a);
+          tmask |= 1u << t;
+          if (++j < n) {
+            sj = sl[j];
+            tj = sj / P.topk;
+          } else {
+            tj = -1;
+          }
         }
       }
-      const float r = epi_reduce16<true>(S, am, et, n);
-      if (et < n) P.aamax[m->slots[m->off[e] + et] * (P.I / 128) + U.tile] = r;
+      const float r = epi_reduce16_mask<true>(S, am, et, tmask);
+      if (et < kMaxT && ((tmask >> et) & 1u))
+        P.aamax[sl[__popc(tmask & ((1u << et) - 1u))] * (P.I / 128) + U.tile] = r;
       // the expert's last finished gate/up tile computes the NVFP4 row scales
-      // of its SwiGLU rows and releases them to the down units
+      // of its SwiGLU rows, quantises the rows once into the expert's image
+      // and releases it to the down units
       epi_sync();
       if (et == 0) {
         const uint32_t old = atom_add_acq_rel(P.exp_sync + e, 1u);
@@ -1403,11 +1493,17 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
       epi_sync();
       if (m->flag) {
         if (et < n) {
-          const int s = m->slots[m->off[e] + et];
+          const int s = sl[et];
           float a = 0.f;
-          for (int j = 0; j < P.I / 128; ++j) a = fmaxf(a, __ldcg(P.aamax + s * (P.I / 128) + j));
-          P.srow_a[s] = a > 0.f ? __fdiv_rn(a, 2688.0f) : 1.0f;
+          for (int jj = 0; jj < P.I / 128; ++jj) a = fmaxf(a, __ldcg(P.aamax + s * (P.I / 128) + jj));
+          const float sr = a > 0.f ? __fdiv_rn(a, 2688.0f) : 1.0f;
+          P.srow_a[s] = sr;
+          m->srow_q[et] = sr;
         }
+        epi_sync();
+        const int ld = P.I;
+        quantize_image(P.aq_img + static_cast<size_t>(e) * image_bytes(P.I), n, P.I, m->srow_q, P.a_buf,
+                       [sl, ld](int i) { return static_cast<size_t>(sl[i]) * ld; }, et);
         epi_sync();
         if (et == 0) st_release(P.exp_sync + kMaxE + e, m->epoch + 1u);
       }
@@ -1480,11 +1576,24 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
   }
   epi_bf16_final(P, S, ph, U, et, g, u);
   if (ph == PH_QKV) {
-    // this tile's q, k and v rows are final: count it in for its groups
+    // this tile's q, k and v rows are final: count it in for its groups (a
+    // counter that grows by grp_tiles per launch; no reply is waited for)
     epi_sync();
     if (et == 0) {
       for (int gg = 0; gg < P.Hkv; ++gg)
-        if (tile_in_group(P, U.tile, gg)) grp_count_in(P, 0, gg, P.grp_tiles[gg], m->epoch);
+        if (tile_in_group(P, U.tile, gg)) red_release_add(grp_ctr(P, 0, gg), 1u);
+    }
+  }
+  if (ph == PH_RP && P.moe && !U.router) {
+    // the last finished pooler tile announces that p and its amax partials
+    // are complete (every CTA then quantises a share of the p image)
+    epi_sync();
+    if (et == 0) {
+      const uint32_t old = atom_add_acq_rel(P.misc_ctr + 1, 1u);
+      if (old == static_cast<uint32_t>(P.tiles_pool - 1)) {
+        P.misc_ctr[1] = 0;  // this launch's arrivals are all in
+        st_release(P.misc_ctr + 2, m->epoch + 1u);
+      }
     }
   }
   if (ph == PH_RP && P.moe && U.router) {
@@ -1856,7 +1965,8 @@ MK_DEV void run_epilogue(const LayerParams& P, const Smem& S, uint32_t epoch) {
       for (int u = first_unit(P, ph); u < n && ok; u += P.grid) {
         const int g = u / P.attn_chunks, c = u % P.attn_chunks;
         if (P.first_layer &&
-            !(ok = group_flag_wait(P, S, grp_flag(P, 0, g), epoch + 1u, et == 0, kBarEpi, 128, 1)))
+            !(ok = group_flag_wait(P, S, grp_ctr(P, 0, g), (epoch + 1u) * P.grp_tiles[g], et == 0, kBarEpi,
+                                   128, 1)))
           break;
         const int lo = P.attn_lo + c * P.attn_chunk_len;
         const int hi = min(P.ctx + P.T, lo + P.attn_chunk_len);
@@ -1905,12 +2015,9 @@ MK_DEV void run_epilogue(const LayerParams& P, const Smem& S, uint32_t epoch) {
     if (ph == PH_GU) {
       if (!(ok = group_mbar_wait(P, S, &m->route_ready, 0, ERR_TIMEOUT_ROUTE, et == 0, kBarEpi, 128, 1)))
         break;
-      if (!(ok = epi_wait(P, S, BAR_RP, target, et))) break;
-      if (et < P.T) {
-        float a = 0.f;
-        for (int j = 0; j < P.P / 128; ++j) a = fmaxf(a, __ldcg(P.pamax + j * kMaxT + et));
-        m->srow_ep[et] = a > 0.f ? __fdiv_rn(a, 2688.0f) : 1.0f;
-      }
+      // p complete: its row scales from the amax partials
+      if (!(ok = group_flag_wait(P, S, P.misc_ctr + 2, epoch + 1u, et == 0, kBarEpi, 128, 1))) break;
+      if (et < P.T) m->srow_ep[et] = p_row_scale(P, et);
       epi_sync();
     } else if (ph == PH_DOWN && P.moe) {
       for (int i = et; i < kMaxT * 16; i += 128) (&m->comb_local[0][0])[i] = 0;
@@ -1988,10 +2095,10 @@ __global__ void __launch_bounds__(kThreads, 1) mk_layer_kernel(const __grid_cons
       mbar_init(&m->uq_full[i], 1);
       mbar_init(&m->uq_empty[i], 6);  // 4 MMA issuers, stager and epilogue leaders
     }
-    for (int i = 0; i < 6; ++i) mbar_init(&m->land[i / 3][i % 3], 1);
+    for (int i = 0; i < 2; ++i) mbar_init(&m->land[i], 1);
     m->abort = 0;
     m->n_act = 0;
-    for (int i = 0; i < 6; ++i) m->land_out[i / 3][i % 3] = 0;
+    for (int i = 0; i < 2; ++i) m->land_out[i] = 0;
     fence_mbar_init();
   }
   if (warp == 1) {

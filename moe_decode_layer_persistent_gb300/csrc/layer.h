@@ -46,7 +46,8 @@ enum BarrierId : int {
   BAR_DOWN = 6,   // z slots and the combined y written
   BAR_X = 7,      // x_out and its sum-of-squares partials written
   BAR_END = 8,    // next layer's q and K/V rows written
-  BAR_ROUTE = 9   // router top-k written (one CTA adds grid)
+  BAR_ROUTE = 9,  // router top-k written (one CTA adds grid)
+  BAR_PQ = 10     // MoE: each CTA's share of the p image written
 };
 
 struct LayerParams {
@@ -116,7 +117,16 @@ struct LayerParams {
                             // last one resets it), [256, 512) expert's SwiGLU rows
                             // and their scales ready (epoch + 1)
   float* srow_a;            // MoE: NVFP4 row scales of the SwiGLU rows [16*k]
-  uint32_t* misc_ctr;       // [0]: router tiles done
+  // MoE: the expert MMAs' token operands, NVFP4-quantised once per launch in
+  // the layout of a shared-memory operand buffer (image_bytes(K) each: codes
+  // in K-blocks of 2048 B -- 16 rows x 128 B, 128-byte swizzle -- then the
+  // 512-byte scale chunks).  pq_img: p of all T tokens (row t = token t), a
+  // 1/grid share by every CTA once p is complete; aq_img [E]: the SwiGLU rows
+  // of expert e in slot order, by the CTA that finishes e's last gate/up tile.
+  uint8_t* pq_img;
+  uint8_t* aq_img;
+  uint32_t* misc_ctr;       // [0]: router tiles done, [1]: pooler tiles done,
+                            // [2]: p and its amax partials complete (epoch + 1)
   uint32_t* sched;          // [PH_COUNT] next unclaimed unit of each phase (reset by CTA 0 at the end)
   int pf_n;                 // MoE: experts prefetched from the previous step (0: off)
   int32_t* pf_list;         // [2][kMaxPf] predicted experts by launch parity, -1 ends a list
@@ -145,6 +155,12 @@ struct LayerParams {
   float* part_o;            // split-K partials of the o-proj (it overlaps the QKV phase)
 };
 constexpr int kTsSlots = 16;
+
+// Bytes of an NVFP4 operand image of K inputs (K-blocks of 256 inputs: 2 KB of
+// codes and 2 KB of scale chunks each).
+__host__ __device__ constexpr uint32_t image_bytes(int K) {
+  return static_cast<uint32_t>((K + 255) / 256) * 4096u;
+}
 constexpr int kTsPerCta = (PH_COUNT + 1) * kTsSlots;
 
 }  // namespace mk

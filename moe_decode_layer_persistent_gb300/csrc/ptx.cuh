@@ -100,6 +100,13 @@ MK_DEV void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Global-memory writes made with ordinary stores (here: by another CTA, then
+// released to this one) are ordered before this thread's later bulk copies
+// (async proxy) of the same memory by this fence.
+MK_DEV void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ----------------------------------------------------------------------- TMA
 MK_DEV void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int32_t x,
                         int32_t y, uint64_t policy) {

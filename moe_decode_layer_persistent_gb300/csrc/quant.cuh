@@ -54,6 +54,19 @@ MK_DEV void load_bf16x16(const __nv_bfloat16* p, float (&x)[16]) {
   }
 }
 
+// The same from global memory written earlier in this launch by other CTAs
+// (loaded from L2, never from the SM's non-coherent L1).
+MK_DEV void load_bf16x16_cg(const __nv_bfloat16* p, float (&x)[16]) {
+  const uint4* q = reinterpret_cast<const uint4*>(p);
+  uint4 a = __ldcg(q), b = __ldcg(q + 1);
+  uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
 // E2M1 codes (two packed words, element 0 in the low nibble) of the
 // correctly rounded quotients x_i / c, without sixteen divisions: with
 // rc = 1/c rounded, x_i * rc lies within 2 ulp of the rounded quotient, so the
@@ -119,6 +132,19 @@ MK_DEV float quantize_row_nvfp4(const __nv_bfloat16* row, int K, Sink& sink) {
     sink.put(b, w0, w1, sb);
   }
   return s_row;
+}
+
+// One 16-element block of a row whose scale s_row is known: E4M3 block scale
+// sb and the E2M1 codes (w0, w1), by the rule above.
+MK_DEV void quantize_block16(const float (&x)[16], float s_row, uint32_t& w0, uint32_t& w1,
+                             uint32_t& sb) {
+  float a16 = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) a16 = fmaxf(a16, fabsf(x[i]));
+  sb = cvt_e4m3(__fdiv_rn(a16, __fmul_rn(6.0f, s_row)));
+  const float sbf = e4m3_to_float(sb);
+  w0 = w1 = 0;
+  if (sbf > 0.f) e2m1_codes16(x, __fmul_rn(sbf, s_row), w0, w1);
 }
 
 // Sink writing row-major codes [K/2] and scales [K/16] (used by self-tests).
