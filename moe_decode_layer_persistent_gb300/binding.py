@@ -108,17 +108,7 @@ _lib_mk_selftest_quantize = _sig("mk_selftest_quantize", _c.c_int,
 _lib_mk_selftest_mma = _sig("mk_selftest_mma", _c.c_int,
                             [_c.c_int32, _vp, _vp, _vp, _vp, _c.c_int32, _vp, _vp])
 
-_lib_mk_selftest_copy_scratch = _sig("mk_selftest_copy_scratch", _c.c_int,
-                                     [_vp, _c.c_int32, _vp, _c.c_size_t])
-
 _lib_mk_get_timestamps = _sig("mk_get_timestamps", _c.c_int, [_vp, _c.c_void_p, _c.c_size_t])
-
-_lib_mk_selftest_stream = _sig("mk_selftest_stream", _c.c_int,
-                               [_vp, _c.c_int32, _c.c_int32, _c.c_int32, _c.c_int32, _c.c_int32,
-                                _c.c_int32, _c.POINTER(_c.c_float), _vp])
-
-_lib_mk_selftest_issue = _sig("mk_selftest_issue", _c.c_int,
-                              [_c.c_int32, _c.c_int32, _c.POINTER(_c.c_longlong)])
 
 _lib_mk_decode_step_noalloc = _sig("mk_decode_step_noalloc", _c.c_int,
                                    [_c.POINTER(mk_layer_config), _c.POINTER(mk_layer_weights),
@@ -128,8 +118,7 @@ EXPORTED = ["mk_layer_create", "mk_decode_step", "mk_decode_step_noalloc", "mk_l
             "mk_layer_destroy", "mk_stack_create", "mk_stack_step", "mk_stack_status",
             "mk_stack_destroy", "mk_status_string", "mk_layer_get_info", "mk_get_timestamps",
             "mk_layer_prefetch_stats", "mk_stack_prefetch_stats",
-            "mk_selftest_quantize", "mk_selftest_mma", "mk_selftest_copy_scratch",
-            "mk_selftest_stream", "mk_selftest_issue"]
+            "mk_selftest_quantize", "mk_selftest_mma"]
 
 
 def _ptr(t):
@@ -296,37 +285,9 @@ def mk_selftest_mma(fp4, a, a_scales, b, b_scales, K, out, stream=None):
         int(fp4), _ptr(a), _ptr(a_scales), _ptr(b), _ptr(b_scales), K, _ptr(out), _stream(stream)))
 
 
-SCRATCH = {"q": 0, "o": 1, "x_mid": 2, "logits": 3, "p": 4, "a": 5, "z": 6, "y": 7, "idx": 8, "w": 9}
-
-
-def mk_selftest_copy_scratch(layer, which, dst):
-    """Copy a library-owned intermediate into the device tensor ``dst``."""
-    w = SCRATCH[which] if isinstance(which, str) else which
-    nbytes = dst.numel() * dst.element_size()
-    _check("mk_selftest_copy_scratch", _lib_mk_selftest_copy_scratch(layer, w, _ptr(dst), nbytes))
-
-
 def mk_get_timestamps(layer, grid):
     """Self-timing stamps of the layer's last step: uint64 array [grid, 10, 16]."""
     import numpy as np
     buf = np.zeros((grid, 10, 16), dtype=np.uint64)
     _check("mk_get_timestamps", _lib_mk_get_timestamps(layer, buf.ctypes.data, buf.size))
     return buf
-
-
-def mk_selftest_stream(w, stages=7, mode=0, ahead=2, grid=None, stream=None):
-    """Time (us) to stream the bf16 matrix ``w`` [rows, K] through TMA tiles."""
-    import torch
-    rows, K = w.shape
-    grid = grid or torch.cuda.get_device_properties(0).multi_processor_count
-    us = _c.c_float()
-    _check("mk_selftest_stream", _lib_mk_selftest_stream(_ptr(w), rows, K, stages, mode, ahead, grid,
-                                                         _c.byref(us), _stream(stream)))
-    return us.value
-
-
-def mk_selftest_issue(what, n):
-    """(issue cycles, completion cycles) of n back-to-back tensor-core instructions."""
-    buf = (_c.c_longlong * 2)()
-    _check("mk_selftest_issue", _lib_mk_selftest_issue(what, n, buf))
-    return buf[0], buf[1]

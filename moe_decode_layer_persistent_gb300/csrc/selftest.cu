@@ -185,234 +185,3 @@ extern "C" mk_status mk_selftest_mma(int32_t fp4, const void* a, const void* a_s
   if (e != cudaSuccess) return MK_ERR_CUDA;
   return h_status ? MK_ERR_TIMEOUT : MK_OK;
 }
-
-// ---------------------------------------------------------------------------
-// Weight-streaming probe: one CTA per SM streams 128-row x 128-byte TMA tiles
-// of a row-major matrix through an mbarrier ring (no math), to measure what
-// the layer's weight path can reach.  mode 0: tiles of (128 rows, k-block),
-// walking k-blocks inside each 128-row group (the layer's order); mode 1: the
-// same plus an L2 prefetch of the tile `ahead` tiles later.
-namespace mk {
-template <int STAGES>
-__global__ void __launch_bounds__(128, 1)
-    k_stream_probe(const __grid_constant__ CUtensorMap tm, int rows, int kblocks, int mode,
-                   int ahead, uint32_t* status, unsigned long long* cycles) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * 16384);
-  uint64_t* empty = full + STAGES;
-  const int groups = (rows + 127) / 128;
-  const int ntiles = groups * kblocks;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    fence_mbar_init();
-  }
-  __syncthreads();
-  const uint64_t timeout = 200ull * 1000 * 1000;
-  const uint64_t t0 = globaltimer();
-  if (threadIdx.x == 0) {
-    const uint64_t pol = policy_evict_first();
-    uint32_t stage = 0, ph = 0;
-    for (int i = blockIdx.x; i < ntiles; i += gridDim.x) {
-      if (!mbar_wait_bounded(&empty[stage], ph ^ 1, timeout)) { atomicExch(status, 1u); break; }
-      mbar_arrive_expect_tx(&full[stage], 16384);
-      const int g = i / kblocks, kb = i % kblocks;
-      tma_load_2d(smem + stage * 16384, &tm, &full[stage], kb * 64, g * 128, pol);
-      if (mode == 1) {
-        const int j = i + ahead * gridDim.x;
-        if (j < ntiles) tma_prefetch_2d(&tm, (j % kblocks) * 64, (j / kblocks) * 128);
-      }
-      if (++stage == STAGES) { stage = 0; ph ^= 1; }
-    }
-  } else if (threadIdx.x == 32) {
-    uint32_t stage = 0, ph = 0;
-    for (int i = blockIdx.x; i < ntiles; i += gridDim.x) {
-      if (!mbar_wait_bounded(&full[stage], ph, timeout)) { atomicExch(status, 2u); break; }
-      mbar_arrive(&empty[stage]);
-      if (++stage == STAGES) { stage = 0; ph ^= 1; }
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) atomicMax(cycles, static_cast<unsigned long long>(globaltimer() - t0));
-}
-}  // namespace mk
-
-extern "C" mk_status mk_selftest_stream(const void* w, int32_t rows, int32_t K, int32_t stages,
-                                        int32_t mode, int32_t ahead, int32_t grid, float* out_us,
-                                        void* stream) {
-  if (!w || rows <= 0 || K <= 0 || K % 64 || !out_us || grid <= 0) return MK_ERR_INVALID_ARG;
-  if (stages != 4 && stages != 7 && stages != 12) return MK_ERR_INVALID_ARG;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  CUtensorMap map;
-  mk_status st = encode_tmap_2d(&map, w, 2, K, rows, 64, 128);
-  if (st != MK_OK) return st;
-  uint32_t* status = nullptr;
-  unsigned long long* cyc = nullptr;
-  MK_CUDA_TRY(cudaMalloc(&status, 16));
-  MK_CUDA_TRY(cudaMalloc(&cyc, 16));
-  cudaMemsetAsync(status, 0, 16, s);
-  cudaMemsetAsync(cyc, 0, 16, s);
-  const size_t smem = 1024 + stages * 16384 + 2 * stages * 8;
-  cudaError_t e = cudaSuccess;
-#define MK_PROBE(NS)                                                                         \
-  if (stages == NS) {                                                                        \
-    cudaFuncSetAttribute(k_stream_probe<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,    \
-                         (int)smem);                                                         \
-    k_stream_probe<NS><<<grid, 128, smem, s>>>(map, rows, K / 64, mode, ahead, status, cyc); \
-  }
-  MK_PROBE(4) MK_PROBE(7) MK_PROBE(12)
-#undef MK_PROBE
-  e = cudaGetLastError();
-  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-  unsigned long long hc = 0;
-  uint32_t hs = 0;
-  if (e == cudaSuccess) e = cudaMemcpy(&hc, cyc, 8, cudaMemcpyDeviceToHost);
-  if (e == cudaSuccess) e = cudaMemcpy(&hs, status, 4, cudaMemcpyDeviceToHost);
-  cudaFree(status);
-  cudaFree(cyc);
-  if (e != cudaSuccess) return MK_ERR_CUDA;
-  *out_us = static_cast<float>(hc) / 1000.0f;
-  return hs ? MK_ERR_TIMEOUT : MK_OK;
-}
-
-// ---------------------------------------------------------------------------
-// Issue-rate probe: one thread issues `n` tcgen05 instructions back to back on
-// a resident shared-memory tile (values irrelevant) and commits once.
-// what: 0 bf16 MMA M128 x N16 x K16, 1 bf16 MMA N64, 2 bf16 MMA N256,
-//       3 NVFP4 block-scaled MMA N16 (K64), 4 tcgen05.cp 32x128b.warpx4,
-//       5 NVFP4 MMA N16 + 2 scale copies per MMA.
-// cycles[0] = clock64 ticks to issue, cycles[1] = ticks until the commit lands.
-namespace mk {
-__global__ void __launch_bounds__(128, 1) k_issue_probe(int what, int n, long long* cycles,
-                                                        uint32_t* status) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + 65536);
-  uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
-  for (int i = threadIdx.x; i < 65536 / 16; i += blockDim.x)
-    reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
-  if (threadIdx.x == 0) {
-    mbar_init(bar, 1);
-    fence_mbar_init();
-  }
-  if (threadIdx.x < 32) {
-    tmem_alloc(slot, 512);
-    tmem_relinquish();
-  }
-  fence_proxy_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tb = *slot;
-  if (what >= 15) {
-    // one warp, several lanes issue in the same instruction: lane l < nl uses
-    // accumulator l
-    const int nl = what == 15 ? 4 : 2;
-    __syncthreads();
-    long long c0 = clock64();
-    if (threadIdx.x < nl) {
-      const uint64_t da = sdesc_kmajor_sw128(smem_u32(smem));
-      const uint64_t db = sdesc_kmajor_sw128(smem_u32(smem + 32768));
-      for (int i = 0; i < n / nl; ++i)
-        mma_nvf4(tb + 32 * threadIdx.x, da, db, idesc_nvf4(128, 16), tb + 256, tb + 260, i != 0);
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      const long long c1 = clock64();
-      mma_commit(bar);
-      if (!mbar_wait_bounded(bar, 0, 100ull * 1000 * 1000)) atomicExch(status, 1u);
-      cycles[0] = c1 - c0;
-      cycles[1] = clock64() - c0;
-    }
-  } else if (what >= 11) {
-    // several warps issue at once: warp w issues n / nw NVFP4 MMAs (or bf16
-    // for what 13/14) into its own accumulator
-    const int nw = (what == 11 || what == 13) ? 2 : 4;
-    const int w = threadIdx.x >> 5;
-    __syncthreads();
-    long long c0 = clock64();
-    if (w < nw && lane_id() == 0) {
-      const uint64_t da = sdesc_kmajor_sw128(smem_u32(smem));
-      const uint64_t db = sdesc_kmajor_sw128(smem_u32(smem + 32768));
-      for (int i = 0; i < n / nw; ++i) {
-        if (what <= 12) mma_nvf4(tb + 32 * w, da, db, idesc_nvf4(128, 16), tb + 256, tb + 260, i != 0);
-        else mma_bf16(tb + 32 * w, da, db, idesc_bf16(128, 16), i != 0);
-      }
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      const long long c1 = clock64();
-      mma_commit(bar);
-      if (!mbar_wait_bounded(bar, 0, 100ull * 1000 * 1000)) atomicExch(status, 1u);
-      cycles[0] = c1 - c0;
-      cycles[1] = clock64() - c0;
-    }
-  } else if (threadIdx.x == 0) {
-    const uint64_t da = sdesc_kmajor_sw128(smem_u32(smem));
-    const uint64_t db = sdesc_kmajor_sw128(smem_u32(smem + 32768));
-    const uint64_t dsf = sdesc_sf_chunk(smem_u32(smem + 49152));
-    const int N = what == 1 ? 64 : (what == 2 ? 256 : 16);
-    const long long c0 = clock64();
-    for (int i = 0; i < n; ++i) {
-      switch (what) {
-        case 0: case 1: case 2: mma_bf16(tb, da, db, idesc_bf16(128, N), i != 0); break;
-        case 3: mma_nvf4(tb, da, db, idesc_nvf4(128, 16), tb + 256, tb + 260, i != 0); break;
-        case 4: tmem_cp_sf(tb + 256 + 4 * (i & 7), dsf); break;
-        case 5:
-          tmem_cp_sf(tb + 256 + 4 * (i & 3), dsf);
-          tmem_cp_sf(tb + 288 + 4 * (i & 3), dsf);
-          mma_nvf4(tb, da, db, idesc_nvf4(128, 16), tb + 256 + 4 * (i & 3), tb + 288 + 4 * (i & 3),
-                   i != 0);
-          break;
-        case 6: mma_bf16(tb + 16 * (i & 7), da, db, idesc_bf16(128, 16), i >= 8); break;
-        case 7:
-          mma_nvf4(tb + 16 * (i & 7), da, db, idesc_nvf4(128, 16), tb + 256, tb + 260, i >= 8);
-          break;
-        case 8: tmem_cp_128x128b(tb + 256 + 4 * (i & 7), sdesc_interleave(smem_u32(smem + 49152), 128, 128)); break;
-        case 9: tmem_cp_128x256b(tb + 256 + 8 * (i & 7), sdesc_interleave(smem_u32(smem + 49152), 2048, 128)); break;
-        case 10:
-          mma_nvf4(tb + 16 * (i & 3), da, db, idesc_nvf4(128, 16), tb + 256, tb + 260, i >= 4);
-          break;
-      }
-    }
-    const long long c1 = clock64();
-    mma_commit(bar);
-    if (!mbar_wait_bounded(bar, 0, 100ull * 1000 * 1000)) atomicExch(status, 1u);
-    const long long c2 = clock64();
-    cycles[0] = c1 - c0;
-    cycles[1] = c2 - c0;
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    tc_fence_after();
-    tmem_dealloc(tb, 512);
-  }
-}
-}  // namespace mk
-
-extern "C" mk_status mk_selftest_issue(int32_t what, int32_t n, long long* host_cycles) {
-  if (what < 0 || what > 16 || n <= 0 || !host_cycles) return MK_ERR_INVALID_ARG;
-  long long* d = nullptr;
-  uint32_t* st = nullptr;
-  MK_CUDA_TRY(cudaMalloc(&d, 16));
-  MK_CUDA_TRY(cudaMalloc(&st, 4));
-  cudaMemset(st, 0, 4);
-  const int smem = 65536 + 1024 + 64;
-  cudaFuncSetAttribute(k_issue_probe, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  k_issue_probe<<<1, 128, smem>>>(what, n, d, st);
-  cudaError_t e = cudaGetLastError();
-  if (e == cudaSuccess) e = cudaDeviceSynchronize();
-  uint32_t hs = 0;
-  if (e == cudaSuccess) e = cudaMemcpy(host_cycles, d, 16, cudaMemcpyDeviceToHost);
-  if (e == cudaSuccess) e = cudaMemcpy(&hs, st, 4, cudaMemcpyDeviceToHost);
-  cudaFree(d);
-  cudaFree(st);
-  if (e != cudaSuccess) return MK_ERR_CUDA;
-  return hs ? MK_ERR_TIMEOUT : MK_OK;
-}
