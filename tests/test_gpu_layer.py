@@ -73,6 +73,7 @@ def test_layer_with_q_in(cuda_lib):
     kc, vc = (oio.np64(t) for t in work["caches"][0])
     r = ol.layer_forward(oio.oracle_cfg(c), Wn, oio.np64(work["x_in"]), kc, vc, ctx,
                          q_in=oio.np64(q_in), first_layer=False)
+    r["router_abs"] = H.router_abs(r, Wn["w_router"])
     H.compare_single(g, r, T, ctx)
 
 

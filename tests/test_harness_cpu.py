@@ -29,18 +29,23 @@ def test_router_check_accepts_reordered_ties_only():
     logits[0, :4] = [3.0, 2.0, 2.0000002, 1.0]
     r_idx = np.array([[0, 2, 1]])                      # oracle order
     r_w = np.array([[0.5, 0.3, 0.2]])
-    # the two near-equal logits swapped: admissible
-    H.check_router(np.array([[0, 1, 2]]), np.array([[0.5, 0.2, 0.3]]), r_idx, r_w, logits)
+    # sum |h w| = 0.01 per logit: slack = 2 (32 u 0.01 + u 2) = 2.6e-7
+    abs_sum = np.full((1, 6), 0.01)
+    # the two near-equal logits (2e-7 apart) swapped: admissible
+    H.check_router(np.array([[0, 1, 2]]), np.array([[0.5, 0.2, 0.3]]), r_idx, r_w, logits, abs_sum)
+    # with larger products the slack grows, but stays far below 1: still admissible
+    H.check_router(np.array([[0, 1, 2]]), np.array([[0.5, 0.2, 0.3]]), r_idx, r_w, logits,
+                   np.full((1, 6), 40.0))
     # a clearly larger logit placed after a smaller one: rejected
     try:
-        H.check_router(np.array([[1, 0, 2]]), np.array([[0.2, 0.5, 0.3]]), r_idx, r_w, logits)
+        H.check_router(np.array([[1, 0, 2]]), np.array([[0.2, 0.5, 0.3]]), r_idx, r_w, logits, abs_sum)
     except AssertionError:
         pass
     else:
         raise AssertionError("a reordering of clearly separated logits must be rejected")
     # a different set: rejected
     try:
-        H.check_router(np.array([[0, 2, 3]]), np.array([[0.5, 0.3, 0.2]]), r_idx, r_w, logits)
+        H.check_router(np.array([[0, 2, 3]]), np.array([[0.5, 0.3, 0.2]]), r_idx, r_w, logits, abs_sum)
     except AssertionError:
         return
     raise AssertionError("a different expert set must be rejected")
