@@ -88,21 +88,56 @@ def visible_range(pos, window):
     return lo, pos
 
 
-def attention(q, k_cache, v_cache, ctx, window):
+def chain_tree(T):
+    """The causal chain as a token tree: token i's ancestors are 0 .. i-1."""
+    return [(1 << (i + 1)) - 1 for i in range(T)]
+
+
+def tree_depths(tree):
+    """Depth of each verify token in a token tree: the number of its ancestors.
+    tree[i] has bit j set iff verify token j is i itself or an ancestor of i
+    (tokens in topological order: ancestors come first)."""
+    return [bin(int(m)).count("1") - 1 for m in tree]
+
+
+def visible_keys(i, ctx, window, tree):
+    """Cache positions visible to verify token i, ascending.
+
+    Token-tree verification ([EXPL] "What the README says the kernels do":
+    the draft proposes a tree of candidates instead of a chain; ORCA "The
+    draft model got faster too": 16 tokens verified): verify token i sits at
+    sequence position ctx + depth_i and its K/V row at cache position ctx + i.
+    It sees the committed prefix j < ctx within the window counted from its
+    sequence position (ctx + depth_i - j < window), and each verify token j
+    that is i or an ancestor of i, within the window counted in depth
+    (depth_i - depth_j < window).  For the chain, depth_i = i and this is the
+    causal rule: key j visible iff j <= ctx + i and ctx + i - j < window."""
+    depth = tree_depths(tree)
+    lo, _ = visible_range(ctx + depth[i], window)
+    keys = list(range(lo, ctx))
+    for j in range(i + 1):
+        if (int(tree[i]) >> j) & 1 and (window == 0 or depth[i] - depth[j] < window):
+            keys.append(ctx + j)
+    return keys
+
+
+def attention(q, k_cache, v_cache, ctx, window, tree=None):
     """Step 2.  q [T, Hq, d]; caches [>= ctx+T, Hkv, d] holding the new rows.
 
-    Verify token i sits at position ctx + i.  Returns o [T, Hq, d] (float64,
-    not rounded)."""
+    Verify token i sees the keys visible_keys(i, ...) gives; tree = None is
+    the causal chain (token i at position ctx + i).  Returns o [T, Hq, d]
+    (float64, not rounded)."""
     T, Hq, d = q.shape
     Hkv = k_cache.shape[1]
     group = Hq // Hkv
     o = np.zeros((T, Hq, d))
     scale = 1.0 / math.sqrt(d)
+    tree = chain_tree(T) if tree is None else tree
     for i in range(T):
-        lo, hi = visible_range(ctx + i, window)
+        keys = visible_keys(i, ctx, window, tree)
         for g in range(Hkv):
-            K = np.asarray(k_cache[lo:hi + 1, g, :], dtype=np.float64)
-            V = np.asarray(v_cache[lo:hi + 1, g, :], dtype=np.float64)
+            K = np.asarray(k_cache[keys, g, :], dtype=np.float64)
+            V = np.asarray(v_cache[keys, g, :], dtype=np.float64)
             Q = q[i, g * group:(g + 1) * group, :]
             s = (Q @ K.T) * scale                       # [group, n]
             s = s - s.max(axis=1, keepdims=True)
@@ -206,7 +241,7 @@ def dense_ffn(h, W):
 
 
 def layer_forward(cfg, W, x_in, k_cache, v_cache, ctx, q_in=None, first_layer=True,
-                  next_W=None, next_k_cache=None, next_v_cache=None, renorm=False):
+                  next_W=None, next_k_cache=None, next_v_cache=None, renorm=False, tree=None):
     """One layer launch's worth of work.
 
     cfg: dict with n_q_heads, n_kv_heads, head_dim, window, ffn ('moe'|'dense'),
@@ -217,6 +252,7 @@ def layer_forward(cfg, W, x_in, k_cache, v_cache, ctx, q_in=None, first_layer=Tr
          the caches must already hold rows ctx .. ctx+T-1.
     next_W: if given, step 11 with next_W's attn_norm_w and w_qkv, writing
          rows ctx .. ctx+T-1 of copies of next_k_cache / next_v_cache.
+    tree: token-tree masks (see visible_keys); None = the causal chain.
     Returns a dict of every intermediate (bf16 values as float64 arrays).
     """
     eps = cfg.get("eps", RMS_EPS)
@@ -234,7 +270,7 @@ def layer_forward(cfg, W, x_in, k_cache, v_cache, ctx, q_in=None, first_layer=Tr
     else:
         q = np.asarray(q_in, dtype=np.float64).reshape(T, Hq, d)
     out["q"] = q
-    o = bf16_round(attention(q, kc, vc, ctx, cfg["window"])).reshape(T, Hq * d)
+    o = bf16_round(attention(q, kc, vc, ctx, cfg["window"], tree)).reshape(T, Hq * d)
     out["o"] = o
     x_mid = bf16_round(x_in + o @ np.asarray(W["w_o"], dtype=np.float64).T)
     out["x_mid"] = x_mid
@@ -265,7 +301,7 @@ def layer_forward(cfg, W, x_in, k_cache, v_cache, ctx, q_in=None, first_layer=Tr
     return out
 
 
-def stack_forward(cfgs, Ws, x_in, k_caches, v_caches, ctx, renorm=False, keep=None):
+def stack_forward(cfgs, Ws, x_in, k_caches, v_caches, ctx, renorm=False, keep=None, tree=None):
     """A chain of layers: layer 0 runs step 1 itself, layer l < L-1 fuses layer
     l+1's step 1, the last layer has no next QKV.  Returns (x_out, per-layer
     list of dicts restricted to the keys in ``keep``), and the updated caches.
@@ -283,7 +319,7 @@ def stack_forward(cfgs, Ws, x_in, k_caches, v_caches, ctx, renorm=False, keep=No
                           first_layer=(l == 0), next_W=nxt,
                           next_k_cache=kcs[l + 1] if nxt is not None else None,
                           next_v_cache=vcs[l + 1] if nxt is not None else None,
-                          renorm=renorm)
+                          renorm=renorm, tree=tree)
         kcs[l] = r["k_cache"]
         vcs[l] = r["v_cache"]
         if nxt is not None:

@@ -176,6 +176,101 @@ def test_router_softmax_and_weights():
     assert np.array_equal(logits, (h @ wr.T).astype(np.float32))
 
 
+# ------------------------------------------------------ token-tree attention ---
+
+# A 16-token tree in topological order, written as parent indices (-1: the
+# root, i.e. the token after the committed prefix): a root with three
+# branches, branches of different depth, siblings at several levels.
+TREE_PARENTS = [-1, 0, 0, 0, 1, 1, 2, 4, 4, 5, 6, 7, 3, 12, 9, 13]
+
+
+def tree_masks(parents):
+    """Ancestor-or-self bitmasks from parent indices (independent of the oracle)."""
+    m = []
+    for i, p in enumerate(parents):
+        m.append((1 << i) | (m[p] if p >= 0 else 0))
+    return m
+
+
+def test_tree_masks_of_a_chain_and_of_the_test_tree():
+    assert ol.chain_tree(4) == tree_masks([-1, 0, 1, 2]) == [1, 3, 7, 15]
+    m = tree_masks(TREE_PARENTS)
+    assert ol.tree_depths(m)[:7] == [0, 1, 1, 1, 2, 2, 2]
+    assert ol.tree_depths(m)[15] == 4             # 15 -> 13 -> 12 -> 3 -> 0
+
+
+@pytest.mark.parametrize("window", [0, 5, 3, 2048])
+def test_tree_chain_mask_equals_the_causal_chain(window):
+    """The chain given as a tree reproduces the causal attention bit for bit,
+    also with windows shorter than the verify tokens."""
+    rng = np.random.default_rng(30)
+    T, ctx = 16, 23
+    q = bf(rng, T, 4, 8)
+    kc = bf(rng, ctx + T, 2, 8)
+    vc = bf(rng, ctx + T, 2, 8)
+    assert np.array_equal(ol.attention(q, kc, vc, ctx, window, tree_masks(list(range(-1, T - 1)))),
+                          ol.attention(q, kc, vc, ctx, window))
+
+
+@pytest.mark.parametrize("window", [0, 9])
+def test_tree_token_equals_chain_attention_over_its_path(window):
+    """Verify token i of a tree attends exactly like the last token of the
+    causal chain made of the prefix and i's root-to-i path: rebuild that chain
+    (its rows at positions ctx .. ctx + depth_i) and compare bit for bit."""
+    rng = np.random.default_rng(31)
+    T, ctx, Hq, Hkv, d = len(TREE_PARENTS), 12, 4, 2, 8
+    q = bf(rng, T, Hq, d)
+    kc = bf(rng, ctx + T, Hkv, d)
+    vc = bf(rng, ctx + T, Hkv, d)
+    got = ol.attention(q, kc, vc, ctx, window, tree_masks(TREE_PARENTS))
+    for i in range(T):
+        path = []
+        j = i
+        while j >= 0:
+            path.append(j)
+            j = TREE_PARENTS[j]
+        path.reverse()
+        kp = np.concatenate([kc[:ctx], kc[[ctx + j for j in path]]])
+        vp = np.concatenate([vc[:ctx], vc[[ctx + j for j in path]]])
+        qp = np.zeros((len(path), Hq, d))
+        qp[-1] = q[i]
+        chain = ol.attention(qp, kp, vp, ctx, window)
+        assert np.array_equal(got[i], chain[-1]), i
+
+
+def test_tree_attention_brute_force_and_siblings_unseen():
+    """Textbook loop over the visible keys of a small tree; changing a token
+    that is not an ancestor of i leaves i's output unchanged."""
+    rng = np.random.default_rng(32)
+    parents = [-1, 0, 0, 1, 2]
+    T, ctx, W, Hq, Hkv, d = 5, 6, 4, 2, 1, 3
+    m = tree_masks(parents)
+    depth = [0, 1, 1, 2, 2]
+    q = bf(rng, T, Hq, d)
+    kc = bf(rng, ctx + T, Hkv, d)
+    vc = bf(rng, ctx + T, Hkv, d)
+    got = ol.attention(q, kc, vc, ctx, W, m)
+    for i in range(T):
+        pos = ctx + depth[i]
+        js = [j for j in range(ctx) if pos - j < W]
+        js += [ctx + j for j in range(T) if (m[i] >> j) & 1 and depth[i] - depth[j] < W]
+        for h in range(Hq):
+            sc = [sum(q[i, h, c] * kc[j, 0, c] for c in range(d)) / math.sqrt(d) for j in js]
+            mx = max(sc)
+            ws = [math.exp(s - mx) for s in sc]
+            for c in range(d):
+                want = sum(w * vc[j, 0, c] for w, j in zip(ws, js)) / sum(ws)
+                assert abs(got[i, h, c] - want) < 1e-12
+    kc2, vc2 = kc.copy(), vc.copy()
+    kc2[ctx + 2] += 1.0                       # token 2: not an ancestor of 1 or 3
+    vc2[ctx + 2] -= 1.0
+    other = ol.attention(q, kc2, vc2, ctx, W, m)
+    for i in (0, 1, 3):
+        assert np.array_equal(other[i], got[i])
+    for i in (2, 4):
+        assert not np.array_equal(other[i], got[i])
+
+
 # -------------------------------------------------------------------- MoE ---
 
 def _moe_weights(rng, E, H, P, I):
