@@ -39,11 +39,11 @@ top-k only when ``renorm`` is set); pooler and unpooler are plain linear maps.
 Dense variant (draft layers, [AIC] "Key Takeaways" / ORCA "The draft model got
 faster too": Qwen3-style GQA layers): steps 4-10 become
   h = bf16(RMSNorm(x_mid) * g2); a = bf16(SiLU(h W_g^T) * (h W_u^T));
-  y = bf16(a W_d^T); x_out = bf16(x_mid + y).
-The MLP output y is a bf16 activation before the residual add, like every
-other op output of the layer ("bf16 activations"); the MoE branch's unpooler
-output is not (step 10 adds it to x_mid before the one rounding), because the
-unpooler is the projection that ends the FFN there, as W_o ends attention.
+  x_out = bf16(x_mid + a W_d^T).
+The down projection's output is added to the residual before its one
+rounding, as the o-proj (step 3) and the unpooler (step 10) are: rounding it
+to bf16 first would add a second rounding after which x_out depends on which
+side of a bf16 boundary each product lands.
 
 Weight layouts (all "output rows x input columns", input contiguous):
   w_qkv [Hq*d + 2*Hkv*d, H] (q heads, then k heads, then v heads), w_o [H, Hq*d],
@@ -233,11 +233,12 @@ def moe_ffn(h, W, idx, w):
 
 
 def dense_ffn(h, W):
-    """Steps 6-10 of the dense variant: the SwiGLU MLP output y (bf16 values)."""
+    """Steps 6-10 of the dense variant: the SwiGLU activation a (bf16 values)
+    and the down projection's output before the residual (not rounded)."""
     g = h @ np.asarray(W["w_gate"], dtype=np.float64).T
     u = h @ np.asarray(W["w_up"], dtype=np.float64).T
     a = bf16_round(silu(g) * u)
-    return dict(a=a, y=bf16_round(a @ np.asarray(W["w_down"], dtype=np.float64).T))
+    return dict(a=a, ffn_out=a @ np.asarray(W["w_down"], dtype=np.float64).T)
 
 
 def layer_forward(cfg, W, x_in, k_cache, v_cache, ctx, q_in=None, first_layer=True,
@@ -286,8 +287,7 @@ def layer_forward(cfg, W, x_in, k_cache, v_cache, ctx, q_in=None, first_layer=Tr
     else:
         dres = dense_ffn(h, W)
         out["a"] = dres["a"]
-        out["y"] = dres["y"]
-        x_out = bf16_round(x_mid + dres["y"])
+        x_out = bf16_round(x_mid + dres["ffn_out"])
     out["x_out"] = x_out
     out["k_cache"] = kc
     out["v_cache"] = vc

@@ -400,7 +400,7 @@ def _torch_layer(cfg, W, x, kc, vc, ctx):
     h = r16(F.rms_norm(x_mid, (H,), t(W["ffn_norm_w"]), eps=1e-6))
     if cfg["ffn"] == "dense":
         a = r16(F.silu(F.linear(h, t(W["w_gate"]))) * F.linear(h, t(W["w_up"])))
-        return r16(x_mid + r16(F.linear(a, t(W["w_down"])))).numpy(), None
+        return r16(x_mid + F.linear(a, t(W["w_down"]))).numpy(), None
     logits = F.linear(h, t(W["w_router"])).float()
     top = torch.topk(logits, cfg["top_k"], dim=1)
     probs = torch.softmax(logits.double(), dim=1)
