@@ -66,6 +66,14 @@ typedef enum {
 #define MK_FIRST_LAYER   0x1u  /* run RMSNorm + QKV + KV write on x_in first     */
 #define MK_FUSE_NEXT_QKV 0x2u  /* end with the next layer's RMSNorm+QKV+KV write */
 #define MK_TOPK_RENORM   0x4u  /* combine weights renormalised over the top-k    */
+#define MK_PREFETCH_NEXT_KV 0x8u /* in a stack (mk_stack_step), fetch the next
+                                    layer's old KV rows -- those its verify tokens
+                                    will see -- into L2 while this layer runs its
+                                    last weight phases (page "Muse Spark Open:
+                                    1,109 Tokens a Second ...", section "What the
+                                    5.9 ms is still spent on": the next layer's
+                                    old KV is prefetched into L2 before its launch
+                                    lands); ignored by mk_decode_step           */
 
 typedef struct mk_layer_config {
   int32_t hidden;         /* H, a multiple of 256                                */
@@ -83,7 +91,8 @@ typedef struct mk_layer_config {
   int32_t max_tokens;     /* <= 16                                               */
   int32_t max_ctx;        /* KV capacity in positions (rows of each cache)       */
   float rms_eps;          /* RMSNorm epsilon; 0 selects 1e-6                      */
-  uint32_t flags;         /* MK_FIRST_LAYER | MK_FUSE_NEXT_QKV | MK_TOPK_RENORM  */
+  uint32_t flags;         /* MK_FIRST_LAYER | MK_FUSE_NEXT_QKV | MK_TOPK_RENORM
+                             | MK_PREFETCH_NEXT_KV                               */
   int32_t prefetch_experts; /* MoE, 0..16: while the router picks this step's
                                experts, the weights of the previous step's N
                                most-used experts are fetched into L2 (page
@@ -140,6 +149,22 @@ typedef struct mk_step_io {
   void* q_out;            /* MK_FUSE_NEXT_QKV: bf16 [T, Hq*d] next layer's q     */
   int32_t* topk_idx_out;  /* optional (may be NULL), MoE: int32 [T, k]           */
   float* topk_w_out;      /* optional (may be NULL), MoE: float [T, k]           */
+  const uint16_t* tree_mask; /* optional HOST pointer to T uint16, read during the
+                             call: token-tree verification (page "sgl-muse-mega:
+                             Meta's Megakernel ...", section "What the README says
+                             the kernels do": the draft's candidates form a
+                             tree).  Bit j of tree_mask[i] is set iff verify
+                             token j is token i itself or an ancestor of i;
+                             tokens in topological order, so every mask holds
+                             bit i and no bit above i, and the ancestors of an
+                             ancestor are in the mask too (MK_ERR_INVALID_ARG
+                             otherwise).  Token i sits at sequence position
+                             ctx + depth_i (depth = its ancestors' count) and
+                             keeps its K/V row at ctx + i; it sees the prefix
+                             positions j < ctx with ctx + depth_i - j < window
+                             and its ancestors-or-self a with depth_i - depth_a
+                             < window (window 0: no limit).  NULL = the causal
+                             chain (token i's ancestors are 0 .. i-1).           */
 } mk_step_io;
 
 typedef struct mk_layer mk_layer;
@@ -183,6 +208,8 @@ typedef struct mk_stack_io {
   void* const* v_caches;      /* host array of n_layers device pointers        */
   int32_t* topk_idx_out;      /* optional: int32 [n_layers, T, k]              */
   float* topk_w_out;          /* optional: float [n_layers, T, k]              */
+  const uint16_t* tree_mask;  /* optional HOST [T]: as mk_step_io.tree_mask, for
+                                 every layer                                   */
 } mk_stack_io;
 
 /* One decode step through every layer: one launch per layer on `stream`,
@@ -233,8 +260,10 @@ mk_status mk_layer_get_info(mk_layer* layer, mk_layer_info* info);
  * stager working, epilogue waiting for an accumulator, epilogue working,
  * MMA issuing) and three more stamps (MMA starts the phase's units, stagers'
  * input dependency met, epilogue starts the phase's units);
- * row 9 starts with (kernel start, inputs ready, kernel end, router top-k
- * start, routing released).  All values are of the last step; stamps of
+ * row 9 starts with (kernel start, inputs ready, kernel end, this CTA's
+ * router top-k start and its routing arrival -- CTAs 0..T-1 select one token
+ * each -- and router logits complete, in the CTA that finished the last
+ * router tile).  All values are of the last step; stamps of
  * unused phases read 0.  Each CTA keeps them in shared memory and writes them
  * out when it exits, so that timing costs little.  Synchronous. */
 mk_status mk_get_timestamps(mk_layer* layer, uint64_t* host_buf, size_t n);

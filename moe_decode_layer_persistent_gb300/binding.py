@@ -24,6 +24,7 @@ MK_FFN_DENSE_SWIGLU_BF16 = 1
 MK_FIRST_LAYER = 0x1
 MK_FUSE_NEXT_QKV = 0x2
 MK_TOPK_RENORM = 0x4
+MK_PREFETCH_NEXT_KV = 0x8
 
 _vp = ctypes.c_void_p
 
@@ -65,13 +66,15 @@ class mk_step_io(ctypes.Structure):
     _fields_ = [("n_tokens", ctypes.c_int32), ("ctx_len", ctypes.c_int32),
                 ("x_in", _vp), ("x_out", _vp), ("q_in", _vp), ("k_cache", _vp),
                 ("v_cache", _vp), ("next_k_cache", _vp), ("next_v_cache", _vp),
-                ("q_out", _vp), ("topk_idx_out", _vp), ("topk_w_out", _vp)]
+                ("q_out", _vp), ("topk_idx_out", _vp), ("topk_w_out", _vp),
+                ("tree_mask", ctypes.POINTER(ctypes.c_uint16))]
 
 
 class mk_stack_io(ctypes.Structure):
     _fields_ = [("n_tokens", ctypes.c_int32), ("ctx_len", ctypes.c_int32),
                 ("x_in", _vp), ("x_out", _vp), ("k_caches", ctypes.POINTER(_vp)),
-                ("v_caches", ctypes.POINTER(_vp)), ("topk_idx_out", _vp), ("topk_w_out", _vp)]
+                ("v_caches", ctypes.POINTER(_vp)), ("topk_idx_out", _vp), ("topk_w_out", _vp),
+                ("tree_mask", ctypes.POINTER(ctypes.c_uint16))]
 
 
 class mk_layer_info(ctypes.Structure):
@@ -183,14 +186,25 @@ def mk_layer_create(cfg, weights):
     return h.value
 
 
+def _tree(io, tree_mask):
+    """Host array of the token-tree masks (kept alive with the io struct)."""
+    if tree_mask is None:
+        return
+    arr = (ctypes.c_uint16 * len(tree_mask))(*[int(m) for m in tree_mask])
+    io.tree_mask = ctypes.cast(arr, ctypes.POINTER(ctypes.c_uint16))
+    io._tree = arr
+
+
 def make_step_io(T, ctx, x_in, x_out, k_cache, v_cache, q_in=None, next_k_cache=None,
-                 next_v_cache=None, q_out=None, topk_idx_out=None, topk_w_out=None):
+                 next_v_cache=None, q_out=None, topk_idx_out=None, topk_w_out=None, tree_mask=None):
+    """tree_mask: optional list of T ancestor-or-self bitmasks (token tree)."""
     io = mk_step_io()
     io.n_tokens, io.ctx_len = T, ctx
     io.x_in, io.x_out, io.q_in = _ptr(x_in), _ptr(x_out), _ptr(q_in)
     io.k_cache, io.v_cache = _ptr(k_cache), _ptr(v_cache)
     io.next_k_cache, io.next_v_cache, io.q_out = _ptr(next_k_cache), _ptr(next_v_cache), _ptr(q_out)
     io.topk_idx_out, io.topk_w_out = _ptr(topk_idx_out), _ptr(topk_w_out)
+    _tree(io, tree_mask)
     return io
 
 
@@ -233,7 +247,8 @@ def mk_stack_create(layers):
     return h.value
 
 
-def make_stack_io(T, ctx, x_in, x_out, k_caches, v_caches, topk_idx_out=None, topk_w_out=None):
+def make_stack_io(T, ctx, x_in, x_out, k_caches, v_caches, topk_idx_out=None, topk_w_out=None,
+                  tree_mask=None):
     io = mk_stack_io()
     io.n_tokens, io.ctx_len = T, ctx
     io.x_in, io.x_out = _ptr(x_in), _ptr(x_out)
@@ -243,6 +258,7 @@ def make_stack_io(T, ctx, x_in, x_out, k_caches, v_caches, topk_idx_out=None, to
     io.v_caches = ctypes.cast(vc, ctypes.POINTER(_vp))
     io._keep = (kc, vc)
     io.topk_idx_out, io.topk_w_out = _ptr(topk_idx_out), _ptr(topk_w_out)
+    _tree(io, tree_mask)
     return io
 
 

@@ -95,7 +95,8 @@ mk_status validate_config(const mk_layer_config* c, const mk_layer_weights* w) {
   if (c->window < 0) return MK_ERR_INVALID_ARG;
   if (c->max_tokens < 1 || c->max_tokens > kMaxT) return MK_ERR_UNSUPPORTED;
   if (c->max_ctx < 1) return MK_ERR_INVALID_ARG;
-  if (c->flags & ~(MK_FIRST_LAYER | MK_FUSE_NEXT_QKV | MK_TOPK_RENORM)) return MK_ERR_INVALID_ARG;
+  if (c->flags & ~(MK_FIRST_LAYER | MK_FUSE_NEXT_QKV | MK_TOPK_RENORM | MK_PREFETCH_NEXT_KV))
+    return MK_ERR_INVALID_ARG;
   if (c->prefetch_experts < 0 || c->prefetch_experts > kMaxPf) return MK_ERR_INVALID_ARG;
   if (c->n_kv_heads > kMaxGroups) return MK_ERR_UNSUPPORTED;
   if (!w->w_qkv && (c->flags & MK_FIRST_LAYER)) return MK_ERR_INVALID_ARG;
@@ -194,6 +195,27 @@ mk_status fill_step(const mk_layer* L, const mk_step_io* io, LayerParams& P) {
   P.q_out = static_cast<__nv_bfloat16*>(io->q_out);
   P.topk_idx_out = io->topk_idx_out;
   P.topk_w_out = io->topk_w_out;
+  // verify-token visibility: the tree's ancestor-or-self masks (validated),
+  // or the causal chain
+  int depth[kMaxT];
+  P.tree = io->tree_mask != nullptr;
+  for (int i = 0; i < kMaxT; ++i) {
+    P.tree_vis[i] = 0;
+    P.tree_depth[i] = 0;
+  }
+  for (int i = 0; i < io->n_tokens; ++i) {
+    const uint32_t m = io->tree_mask ? io->tree_mask[i] : (2u << i) - 1u;
+    if (!((m >> i) & 1u) || (m >> (i + 1)) != 0) return MK_ERR_INVALID_ARG;
+    if (io->tree_mask)  // the ancestors of an ancestor are ancestors
+      for (int j = 0; j < i; ++j)
+        if (((m >> j) & 1u) && (io->tree_mask[j] & ~m) != 0) return MK_ERR_INVALID_ARG;
+    depth[i] = __builtin_popcount(m) - 1;
+    uint32_t vis = 0;
+    for (int j = 0; j <= i; ++j)
+      if (((m >> j) & 1u) && (c.window == 0 || depth[i] - depth[j] < c.window)) vis |= 1u << j;
+    P.tree_vis[i] = static_cast<uint16_t>(vis);
+    P.tree_depth[i] = static_cast<uint8_t>(depth[i]);
+  }
   // split-KV attention: the key range every verify token may see, cut into
   // chunks of a multiple of 64 positions, about one unit per SM
   const int lo = c.window ? std::max(0, io->ctx_len - c.window + 1) : 0;
@@ -520,12 +542,22 @@ mk_status mk_stack_step(mk_stack* S, const mk_stack_io* io, void* stream) {
       s.next_v_cache = io->v_caches[l + 1];
       s.q_out = S->qbuf[l & 1];
     }
+    s.tree_mask = io->tree_mask;
     const int k = L->cfg.ffn_kind == MK_FFN_MOE_NVFP4 ? L->cfg.top_k : 0;
     if (io->topk_idx_out && k)
       s.topk_idx_out = io->topk_idx_out + static_cast<size_t>(l) * io->n_tokens * k;
     if (io->topk_w_out && k) s.topk_w_out = io->topk_w_out + static_cast<size_t>(l) * io->n_tokens * k;
     mk_status st = fill_step(L, &s, params[l]);
     if (st != MK_OK) return st;
+    if ((L->cfg.flags & MK_PREFETCH_NEXT_KV) && l + 1 < n) {
+      // the rows [lo, ctx) the next layer's verify tokens will see
+      const mk_layer_config& nc = S->layers[l + 1]->cfg;
+      const int64_t lo = nc.window ? std::max(0, io->ctx_len - nc.window + 1) : 0;
+      const int64_t row = static_cast<int64_t>(nc.n_kv_heads) * nc.head_dim * 2;
+      params[l].nkv[0] = static_cast<const uint8_t*>(io->k_caches[l + 1]) + lo * row;
+      params[l].nkv[1] = static_cast<const uint8_t*>(io->v_caches[l + 1]) + lo * row;
+      params[l].nkv_bytes = static_cast<uint64_t>(io->ctx_len - lo) * row;
+    }
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   for (int l = 0; l < n; ++l) {

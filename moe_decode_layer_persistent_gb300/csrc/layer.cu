@@ -647,6 +647,19 @@ MK_DEV void prefetch_bookkeeping(const LayerParams& P, const Smem& S, uint32_t e
   }
 }
 
+// L2 prefetch of this CTA's 1/grid share of the next layer's old K and V rows
+// (a stack's MK_PREFETCH_NEXT_KV), in 16 KB pieces.
+MK_DEV void prefetch_next_kv(const LayerParams& P) {
+  constexpr uint64_t kPiece = 16384;
+  const uint64_t pieces = (P.nkv_bytes + kPiece - 1) / kPiece;
+  for (int m = 0; m < 2; ++m)
+    for (uint64_t i = blockIdx.x; i < pieces; i += P.grid) {
+      const uint64_t off = i * kPiece;
+      const uint64_t n = P.nkv_bytes - off < kPiece ? P.nkv_bytes - off : kPiece;
+      bulk_prefetch_l2(P.nkv[m] + off, static_cast<uint32_t>(n & ~15ull));
+    }
+}
+
 // L2 prefetch of this CTA's 1/grid share of a bf16 weight matrix [N][K]
 // (128-row x 64-column tiles of its tensor map).
 MK_DEV void prefetch_share_l2(const LayerParams& P, const CUtensorMap* map, int N, int K) {
@@ -680,6 +693,9 @@ MK_DEV void run_producer(const LayerParams& P, const Smem& S) {
       if (!wait_bar(P, S, &m->route_ready, 0, ERR_TIMEOUT_ROUTE)) { ok = false; break; }
       route_known = true;
     }
+    // the launch's last weight phases before the fused next QKV run from L2
+    // (unpooler) or stream while HBM has room: fetch the next layer's old KV
+    if (P.nkv_bytes && ph == (P.moe ? PH_UNPOOL : PH_DOWN)) prefetch_next_kv(P);
     // The launch's first weight phase starts with one unit per CTA dealt
     // statically (streamed before the previous launch ends); all other units
     // are claimed from the phase's counter, once the previous launch of this
@@ -840,7 +856,9 @@ MK_DEV void issue_bf16(const LayerParams& P, const Smem& S, int ph, const Unit& 
   uint8_t* raw = S.bbuf(buf) + kLandOff;
   uint8_t* graw = raw + kMaxT * U.nkb * 128;
   const uint32_t rowbytes = static_cast<uint32_t>(U.nkb) * 128u;
-  const uint64_t pol = policy_evict_last();
+  // normal priority: each layer of a stack has its own activation buffers,
+  // and evict-last lines of 62 layers would crowd L2
+  const uint64_t pol = policy_evict_normal();
   uint64_t* lb = &S.m->land[buf];
   S.m->land_out[buf] = 1;
   mbar_arrive_expect_tx(lb, P.T * rowbytes + (src.gain ? rowbytes : 0u));
@@ -889,6 +907,66 @@ MK_DEV bool stage_bf16(const LayerParams& P, const Smem& S, int ph, const Unit& 
   return true;
 }
 
+// Router logits as 32-bit keys whose unsigned order is the float order.
+MK_DEV uint32_t order_key(float v) {
+  const uint32_t b = __float_as_uint(v + 0.0f);  // -0 ranks as +0
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+MK_DEV float key_logit(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Router top-k of token t by one warp: the k largest float32 logits
+// (descending, an exact tie going to the lower expert index), the softmax
+// over all experts (maximum subtracted), the combine weights.  Lane l holds
+// experts l + 32 i as order-preserving keys; a round takes the warp's maximum
+// key, then the lowest expert index holding it, and clears that key.
+MK_DEV void topk_token(const LayerParams& P, int t) {
+  constexpr int kI = kMaxE / 32;  // experts per lane
+  const int lane = lane_id();
+  const float* lg = P.logits + static_cast<size_t>(t) * kMaxE;
+  uint32_t k[kI];
+#pragma unroll
+  for (int i = 0; i < kI; ++i) {
+    const int e = lane + 32 * i;
+    k[i] = e < P.E ? order_key(__ldcg(lg + e)) : 0u;  // 0: no expert
+  }
+  uint32_t mk = 0u;
+#pragma unroll
+  for (int i = 0; i < kI; ++i) mk = max(mk, k[i]);
+  const float mx = key_logit(__reduce_max_sync(0xffffffffu, mk));
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < kI; ++i)
+    if (k[i] != 0u) s += __expf(key_logit(k[i]) - mx);
+  s = warp_sum(s);
+  int ek = 0;
+  uint32_t wk = 0u;
+#pragma unroll 1
+  for (int r = 0; r < P.topk; ++r) {
+    uint32_t b = 0u;
+    int ib = 0;
+#pragma unroll
+    for (int i = kI - 1; i >= 0; --i)
+      if (k[i] >= b && k[i] != 0u) { b = k[i]; ib = i; }
+    const uint32_t x = __reduce_max_sync(0xffffffffu, b);
+    const int c = static_cast<int>(__reduce_min_sync(
+        0xffffffffu, (b == x && x != 0u) ? static_cast<uint32_t>(ib * 32 + lane) : 0xffffffffu));
+#pragma unroll
+    for (int i = 0; i < kI; ++i)
+      if ((c & 31) == lane && i == (c >> 5)) k[i] = 0u;
+    if (lane == r) { ek = c; wk = x; }
+  }
+  float wt = lane < P.topk ? __expf(key_logit(wk) - mx) / s : 0.f;
+  if (P.renorm) wt = wt / warp_sum(wt);
+  if (lane < P.topk) {
+    P.idx[t * P.topk + lane] = ek;
+    P.wts[t * P.topk + lane] = wt;
+    if (P.topk_idx_out) P.topk_idx_out[t * P.topk + lane] = ek;
+    if (P.topk_w_out) P.topk_w_out[t * P.topk + lane] = wt;
+  }
+}
+
 // NVFP4 row scale of p's row t (amax over the pooler tiles' partials).
 MK_DEV float p_row_scale(const LayerParams& P, int t) {
   float a = 0.f;
@@ -915,7 +993,6 @@ MK_DEV void p_image_share(const LayerParams& P, const Smem& S, int tid) {
     sink.r = static_cast<uint32_t>(t);
     sink.put(b, w0, w1, sb);
   }
-  fence_proxy_async_global();  // read by every CTA's bulk copies
 }
 
 // Token operand of an NVFP4 expert unit: an operand image quantised once per
@@ -927,7 +1004,7 @@ MK_DEV void issue_image(const LayerParams& P, const Smem& S, const uint8_t* img,
   uint64_t* lb = &S.m->land[buf];
   S.m->land_out[buf] = 1;
   mbar_arrive_expect_tx(lb, 2 * half);
-  const uint64_t pol = policy_evict_last();
+  const uint64_t pol = policy_evict_normal();  // see issue_bf16
   bulk_load(S.bbuf(buf), img, half, lb, pol);
   bulk_load(S.bbuf(buf) + kBSfOff, img + half, half, lb, pol);
 }
@@ -959,7 +1036,9 @@ MK_DEV bool stage_expert_phase(const LayerParams& P, const Smem& S, int ph, uint
     const int key = gu ? -2 : U.expert;
     if (holds[b] != key) {
       if (tid == 0) {
-        fence_proxy_async_global();  // the image was written by ordinary stores of another CTA
+        // the image was written by ordinary stores of other CTAs, released to
+        // this one: order them before this thread's async-proxy copy
+        fence_proxy_async_global();
         issue_image(P, S, gu ? P.pq_img : P.aq_img + static_cast<size_t>(U.expert) * image_bytes(K), K, b);
       }
       if (!group_mbar_wait(P, S, &m->land[b], land_ph[b], ERR_TIMEOUT_B, tid == 0, kBarStage, 64, 0))
@@ -1023,6 +1102,22 @@ MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
   for (int ph = 0; ph < PH_COUNT && ok; ++ph) {
     if (!phase_is_gemm(ph) || !phase_active(P, ph)) continue;
     if (ph == PH_GU) {
+      // the router top-k, one token per CTA: CTA t < T selects token t's
+      // experts with its first stager warp once the logits are complete; the
+      // arrivals add up to grid (CTA 0 adds the CTAs without a token)
+      if (static_cast<int>(blockIdx.x) < P.T) {
+        if (!group_flag_wait(P, S, P.misc_ctr + 3, epoch + 1u, tid == 0, kBarStage, 64, 0)) { ok = false; break; }
+        if (warp == 0) {
+          if (tid == 0) stamp(P, S, PH_COUNT, 3);
+          topk_token(P, blockIdx.x);
+          __syncwarp();  // the lanes' writes precede lane 0's release
+          if (tid == 0) {
+            red_release_add(P.bar_ctr + BAR_ROUTE,
+                            blockIdx.x == 0 ? 1u + static_cast<uint32_t>(P.grid - P.T) : 1u);
+            stamp(P, S, PH_COUNT, 4);
+          }
+        }
+      }
       // once p is complete, this CTA's share of the p image
       if (!group_flag_wait(P, S, P.misc_ctr + 2, epoch + 1u, tid == 0, kBarStage, 64, 0)) { ok = false; break; }
       p_image_share(P, S, tid);
@@ -1246,94 +1341,10 @@ MK_DEV void quantize_image(uint8_t* img, int rows, int K, const float* srow,
       sink.put(i % nblk, w0, w1, sb);
     }
   }
-  fence_proxy_async_global();  // read by other CTAs' bulk copies
+  // (the readers' bulk copies follow their acquire of the release that
+  // publishes the image, and a proxy fence of their own)
 }
 
-
-// Router: top-k of the float32 logits (descending, an exact tie going to the
-// lower expert index), softmax over all experts, combine weights.  Warp w
-// takes tokens w, w+4 together, then w+8, w+12 (their selection steps
-// interleave, hiding each other's latency); lane l holds experts l + 32i as 32-bit
-// order-preserving keys.  A round takes the warp maximum key, then the lowest
-// expert index holding it, and clears that key.
-MK_DEV uint32_t order_key(float v) {
-  const uint32_t b = __float_as_uint(v + 0.0f);  // -0 ranks as +0
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-MK_DEV float key_logit(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-}
-
-// The code runs once per launch on one SM, so its cost is mostly fetching its
-// instructions: loops, not unrolled copies, except over a lane's 8 experts.
-MK_DEV void router_topk(const LayerParams& P, int et) {
-  constexpr int kI = kMaxE / 32;  // experts per lane
-  const int w = et >> 5, lane = lane_id();
-#pragma unroll 1
-  for (int pass = 0; pass < 2; ++pass) {
-    const int t0 = w + 8 * pass, t1 = t0 + 4;  // two tokens per pass
-    if (t0 >= P.T) break;
-    uint32_t k0[kI], k1[kI];
-    const float* l0 = P.logits + static_cast<size_t>(t0) * kMaxE;
-    const float* l1 = P.logits + static_cast<size_t>(t1 < P.T ? t1 : t0) * kMaxE;
-#pragma unroll
-    for (int i = 0; i < kI; ++i) {
-      const int e = lane + 32 * i;
-      k0[i] = e < P.E ? order_key(__ldcg(l0 + e)) : 0u;  // 0: no expert
-      k1[i] = (e < P.E && t1 < P.T) ? order_key(__ldcg(l1 + e)) : 0u;
-    }
-    // softmax denominators (max subtracted)
-    uint32_t m0 = 0u, m1 = 0u;
-#pragma unroll
-    for (int i = 0; i < kI; ++i) { m0 = max(m0, k0[i]); m1 = max(m1, k1[i]); }
-    const float mx0 = key_logit(__reduce_max_sync(0xffffffffu, m0));
-    const float mx1 = key_logit(__reduce_max_sync(0xffffffffu, m1));
-    float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-    for (int i = 0; i < kI; ++i) {
-      if (k0[i] != 0u) s0 += __expf(key_logit(k0[i]) - mx0);
-      if (k1[i] != 0u) s1 += __expf(key_logit(k1[i]) - mx1);
-    }
-    s0 = warp_sum(s0);
-    s1 = warp_sum(s1);
-    int e0 = 0, e1 = 0;
-    uint32_t w0 = 0u, w1 = 0u;
-#pragma unroll 1
-    for (int r = 0; r < P.topk; ++r) {
-      uint32_t b0 = 0u, b1 = 0u;
-      int i0 = 0, i1 = 0;
-#pragma unroll
-      for (int i = kI - 1; i >= 0; --i) {
-        if (k0[i] >= b0 && k0[i] != 0u) { b0 = k0[i]; i0 = i; }
-        if (k1[i] >= b1 && k1[i] != 0u) { b1 = k1[i]; i1 = i; }
-      }
-      const uint32_t x0 = __reduce_max_sync(0xffffffffu, b0), x1 = __reduce_max_sync(0xffffffffu, b1);
-      const int c0 = static_cast<int>(__reduce_min_sync(
-          0xffffffffu, (b0 == x0 && x0 != 0u) ? static_cast<uint32_t>(i0 * 32 + lane) : 0xffffffffu));
-      const int c1 = static_cast<int>(__reduce_min_sync(
-          0xffffffffu, (b1 == x1 && x1 != 0u) ? static_cast<uint32_t>(i1 * 32 + lane) : 0xffffffffu));
-#pragma unroll
-      for (int i = 0; i < kI; ++i) {
-        if ((c0 & 31) == lane && i == (c0 >> 5)) k0[i] = 0u;
-        if ((c1 & 31) == lane && i == (c1 >> 5)) k1[i] = 0u;
-      }
-      if (lane == r) { e0 = c0; w0 = x0; e1 = c1; w1 = x1; }
-    }
-#pragma unroll 1
-    for (int q = 0; q < 2; ++q) {
-      const int t = q ? t1 : t0;
-      const int e = q ? e1 : e0;
-      float wt = lane < P.topk ? __expf(key_logit(q ? w1 : w0) - (q ? mx1 : mx0)) / (q ? s1 : s0) : 0.f;
-      if (P.renorm) wt = wt / warp_sum(wt);
-      if (t < P.T && lane < P.topk) {
-        P.idx[t * P.topk + lane] = e;
-        P.wts[t * P.topk + lane] = wt;
-        if (P.topk_idx_out) P.topk_idx_out[t * P.topk + lane] = e;
-        if (P.topk_w_out) P.topk_w_out[t * P.topk + lane] = wt;
-      }
-    }
-  }
-}
 
 // Final values of one 128-row tile of a bf16 phase: acc[j][t] for the row
 // (feature) f of this thread.
@@ -1360,10 +1371,8 @@ MK_DEV void epi_bf16_final(const LayerParams& P, const Smem& S, int ph, const Un
     case PH_O:
     case PH_UNPOOL:
     case PH_DOWN: {  // residual: x = bf16(res + acc); sum-of-squares partial
-      // (the dense MLP's output is a bf16 activation itself: x = bf16(res + bf16(acc)))
       const __nv_bfloat16* res = ph == PH_O ? P.x_in : P.xmid;
       __nv_bfloat16* dst = ph == PH_O ? P.xmid : P.x_out;
-      const bool round_acc = ph == PH_DOWN;
       // every residual load is issued before the first store: a load may not
       // move past a store that could alias it, so interleaving them would cost
       // one memory round trip per token
@@ -1376,7 +1385,7 @@ MK_DEV void epi_bf16_final(const LayerParams& P, const Smem& S, int ph, const Un
       for (int t = 0; t < kMaxT; ++t) {
         sq[t] = 0.f;
         if (valid && t < P.T) {
-          const float x = round_bf(rv[t] + (round_acc ? round_bf(g[t]) : g[t]));
+          const float x = round_bf(rv[t] + g[t]);
           dst[static_cast<size_t>(t) * P.H + f] = to_bf(x);
           sq[t] = x * x;
         }
@@ -1418,6 +1427,12 @@ MK_DEV void epi_bf16_final(const LayerParams& P, const Smem& S, int ph, const Un
 MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Unit& U,
                           uint32_t b, uint32_t& acc_ph_b, int et) {
   Misc* m = S.m;
+  // an expert unit's tensor scales, loaded while the accumulator is awaited
+  float ts0 = 0.f, ts1 = 0.f;
+  if (U.fp4) {
+    ts0 = __ldg(ph == PH_GU ? P.ts_gate + U.expert : P.ts_down + U.expert);
+    if (ph == PH_GU) ts1 = __ldg(P.ts_up + U.expert);
+  }
   const uint64_t w0 = tnow(P);
   if (!group_mbar_wait(P, S, &m->accfull[b], acc_ph_b, ERR_TIMEOUT_ACC, et == 0, kBarEpi, 128, 1))
     return false;
@@ -1453,7 +1468,7 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
     if (ph == PH_GU) {
       // Accumulator column t is token t (the p image holds every token).  The
       // expert's slots, ascending, name its tokens in ascending order.
-      const float tg = P.ts_gate[e], tu = P.ts_up[e];
+      const float tg = ts0, tu = ts1;
       const int* sl = m->slots + m->off[e];
       float am[kMaxT];
       uint32_t tmask = 0;
@@ -1508,7 +1523,7 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
         if (et == 0) st_release(P.exp_sync + kMaxE + e, m->epoch + 1u);
       }
     } else {
-      const float td = P.ts_down[e];
+      const float td = ts0;
       for (int i = 0; i < n; ++i) {
         const int s = m->slots[m->off[e] + i];
         P.z_buf[static_cast<size_t>(s) * P.P + f] = to_bf(g[i] * m->srow_ep[s] * td);
@@ -1597,24 +1612,15 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
     }
   }
   if (ph == PH_RP && P.moe && U.router) {
-    // the last finished router tile computes the top-k for every token
+    // the last finished router tile announces that the logits are complete
+    // (the first T CTAs then select one token's experts each)
     epi_sync();
     if (et == 0) {
       const uint32_t old = atom_add_acq_rel(P.misc_ctr, 1u);
-      const bool last = old == static_cast<uint32_t>(P.tiles_router - 1);
-      if (last) *P.misc_ctr = 0;  // this launch's arrivals are all in
-      m->flag = last;
-    }
-    epi_sync();
-    if (m->flag) {
-      if (et == 0) stamp(P, S, PH_COUNT, 3);
-      router_topk(P, et);
-      if (et == 0) stamp(P, S, PH_COUNT, 6);
-      epi_sync();
-      if (et == 0) stamp(P, S, PH_COUNT, 7);
-      if (et == 0) {
-        red_release_add(P.bar_ctr + BAR_ROUTE, static_cast<uint32_t>(P.grid));
-        stamp(P, S, PH_COUNT, 4);
+      if (old == static_cast<uint32_t>(P.tiles_router - 1)) {
+        *P.misc_ctr = 0;  // this launch's arrivals are all in
+        st_release(P.misc_ctr + 3, m->epoch + 1u);
+        stamp(P, S, PH_COUNT, 5);
       }
     }
   }
@@ -1661,7 +1667,10 @@ MK_DEV uint32_t tile_off(int r, int c) {
 
 // One unit: KV head g, positions [lo, hi).  Each warp owns q head 4g + w and
 // the T tokens (16 rows); flash-style online softmax in the log2 domain.
-template <int D>
+// kTree: the verify tokens form a token tree (visibility from tree_vis /
+// tree_depth) instead of the causal chain (a separate instance, so that the
+// chain's innermost loop keeps its registers).
+template <int D, bool kTree>
 MK_DEV void attention_unit(const LayerParams& P, const Smem& S, int g, int lo, int hi, int chunk_id,
                            int et) {
   constexpr int kChunks = D / 8;  // 16-byte chunks per row
@@ -1703,7 +1712,14 @@ MK_DEV void attention_unit(const LayerParams& P, const Smem& S, int g, int lo, i
   float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
   const float sl2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
   const int r0 = lane >> 2;            // rows r0 and r0 + 8 of this warp = tokens
-  const int posq[2] = {P.ctx + r0, P.ctx + r0 + 8};
+  // each token's sequence position (prefix window) and, in a tree, its
+  // visible verify tokens
+  const int posq[2] = {P.ctx + (kTree ? P.tree_depth[r0] : r0), P.ctx + (kTree ? P.tree_depth[r0 + 8] : r0 + 8)};
+  uint32_t vism[2] = {0u, 0u};
+  if (kTree) {
+    vism[0] = P.tree_vis[r0];
+    vism[1] = P.tree_vis[r0 + 8];
+  }
 
   const int ntiles = (hi - lo + 63) / 64;
   for (int it = 0; it < ntiles; ++it) {
@@ -1751,8 +1767,14 @@ MK_DEV void attention_unit(const LayerParams& P, const Smem& S, int g, int lo, i
         for (int e = 0; e < 4; ++e) {
           const int j = q0 + nt * 8 + 2 * (lane & 3) + (e & 1);
           const int rr = e >> 1;
+          // chain: key j visible iff j <= the token's position, within the
+          // window; tree: prefix keys by the window from the token's
+          // position, verify tokens by the visibility mask
           const int pq = posq[rr];
-          const bool vis = j < hi && j <= pq && (P.window == 0 || pq - j < P.window);
+          const bool vis =
+              kTree ? j < hi && (j < P.ctx ? (P.window == 0 || pq - j < P.window)
+                                           : ((vism[rr] >> (j - P.ctx)) & 1u) != 0)
+                    : j < hi && j <= pq && (P.window == 0 || pq - j < P.window);
           const float v = vis ? s[nt][e] * sl2 : -INFINITY;
           s[nt][e] = v;
           mx[rr] = fmaxf(mx[rr], v);
@@ -1970,8 +1992,13 @@ MK_DEV void run_epilogue(const LayerParams& P, const Smem& S, uint32_t epoch) {
           break;
         const int lo = P.attn_lo + c * P.attn_chunk_len;
         const int hi = min(P.ctx + P.T, lo + P.attn_chunk_len);
-        if (P.d == 128) attention_unit<128>(P, S, g, lo, hi, c, et);
-        else attention_unit<64>(P, S, g, lo, hi, c, et);
+        if (P.d == 128) {
+          if (P.tree) attention_unit<128, true>(P, S, g, lo, hi, c, et);
+          else attention_unit<128, false>(P, S, g, lo, hi, c, et);
+        } else {
+          if (P.tree) attention_unit<64, true>(P, S, g, lo, hi, c, et);
+          else attention_unit<64, false>(P, S, g, lo, hi, c, et);
+        }
         epi_sync();
         if (et == 0) grp_count_in(P, 1, g, P.attn_chunks, epoch);
       }

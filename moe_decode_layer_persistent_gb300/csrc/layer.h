@@ -73,6 +73,17 @@ struct LayerParams {
   __nv_bfloat16* q_out;
   int32_t* topk_idx_out;
   float* topk_w_out;
+  // attention visibility of the verify tokens (token tree or causal chain):
+  // token t sits at position ctx + tree_depth[t]; bit j of tree_vis[t] =
+  // verify token j is visible to t (ancestor-or-self within the window);
+  // rows t >= T: 0
+  uint16_t tree_vis[kMaxT];
+  uint8_t tree_depth[kMaxT];
+  int tree;                 // 1: a token tree was given (else the causal chain)
+  // stacks (MK_PREFETCH_NEXT_KV): the next layer's old K and V rows, each
+  // one contiguous range of nkv_bytes from nkv[0] / nkv[1] (0: none)
+  const uint8_t* nkv[2];
+  uint64_t nkv_bytes;
 
   // weights used outside TMA
   const __nv_bfloat16* attn_norm_w;
@@ -126,7 +137,8 @@ struct LayerParams {
   uint8_t* pq_img;
   uint8_t* aq_img;
   uint32_t* misc_ctr;       // [0]: router tiles done, [1]: pooler tiles done,
-                            // [2]: p and its amax partials complete (epoch + 1)
+                            // [2]: p and its amax partials complete (epoch + 1),
+                            // [3]: router logits complete (epoch + 1)
   uint32_t* sched;          // [PH_COUNT] next unclaimed unit of each phase (reset by CTA 0 at the end)
   int pf_n;                 // MoE: experts prefetched from the previous step (0: off)
   int32_t* pf_list;         // [2][kMaxPf] predicted experts by launch parity, -1 ends a list

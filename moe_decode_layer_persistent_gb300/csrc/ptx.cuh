@@ -145,6 +145,11 @@ MK_DEV uint64_t policy_evict_last() {
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
+MK_DEV uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
 
 // ------------------------------------------------------- tensor memory / MMA
 MK_DEV void tmem_alloc(uint32_t* result_smem, uint32_t ncols) {

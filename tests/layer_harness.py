@@ -69,7 +69,7 @@ def make_layer(binding, wl, W, flags, max_ctx, next_W=None, window=None, timeout
 
 
 def run_single_layer(binding, work, T=None, ctx=None, fuse_next=False, first_layer=True,
-                     q_in=None, renorm=False, stream=None, keep_layer=False):
+                     q_in=None, renorm=False, stream=None, keep_layer=False, tree_mask=None):
     """One mk_decode_step on device tensors of `work` (a synth.make_workload
     result on cuda).  Returns host copies of every output."""
     wl = work["wl"]
@@ -95,7 +95,8 @@ def run_single_layer(binding, work, T=None, ctx=None, fuse_next=False, first_lay
         q_out = torch.zeros((T, c["n_q_heads"] * c["head_dim"]), dtype=torch.bfloat16, device=dev)
     io = binding.make_step_io(T, ctx, x_in, x_out, kc, vc, q_in=q_in, next_k_cache=nkc,
                               next_v_cache=nvc, q_out=q_out,
-                              topk_idx_out=idx if k else None, topk_w_out=wts if k else None)
+                              topk_idx_out=idx if k else None, topk_w_out=wts if k else None,
+                              tree_mask=tree_mask)
     binding.mk_decode_step(layer, io, stream)
     torch.cuda.synchronize()
     st = binding.mk_layer_status(layer)
@@ -110,7 +111,7 @@ def run_single_layer(binding, work, T=None, ctx=None, fuse_next=False, first_lay
     return out
 
 
-def oracle_single_layer(work, T=None, ctx=None, fuse_next=False, Wn=None, renorm=False):
+def oracle_single_layer(work, T=None, ctx=None, fuse_next=False, Wn=None, renorm=False, tree=None):
     wl = work["wl"]
     c = work["cfgs"][0]
     T = wl["T"] if T is None else T
@@ -123,7 +124,7 @@ def oracle_single_layer(work, T=None, ctx=None, fuse_next=False, Wn=None, renorm
         nxt = oio.np_weights({k: v for k, v in work["next"].items() if k in ("attn_norm_w", "w_qkv")})
         nkc, nvc = oio.np64(work["next"]["k_cache"]), oio.np64(work["next"]["v_cache"])
     r = ol.layer_forward(oio.oracle_cfg(c), Wn, oio.np64(work["x_in"][:T]), kc, vc, ctx,
-                         next_W=nxt, next_k_cache=nkc, next_v_cache=nvc, renorm=renorm)
+                         next_W=nxt, next_k_cache=nkc, next_v_cache=nvc, renorm=renorm, tree=tree)
     if "w_router" in Wn and "logits" in r:
         r["router_abs"] = router_abs(r, Wn["w_router"])
     return r

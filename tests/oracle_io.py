@@ -37,7 +37,7 @@ def router_margin(logits, k):
     return s[:, k - 1] - s[:, k]
 
 
-def enforce_margin_single(work, x_np=None, q_np=None, first_layer=True, max_draws=400):
+def enforce_margin_single(work, x_np=None, q_np=None, first_layer=True, max_draws=400, tree=None):
     """Redraw layer 0's router (draw 0, 1, ...) until every token's gap between
     the k-th and (k+1)-th float32 logit is >= MARGIN.  Mutates work['Ws'][0]
     (torch) and returns the numpy weights and the draw used."""
@@ -58,7 +58,7 @@ def enforce_margin_single(work, x_np=None, q_np=None, first_layer=True, max_draw
     else:
         q = q_np
     from oracle.numerics import bf16_round
-    o = bf16_round(ol.attention(q, kc, vc, wl["ctx"], c["window"])).reshape(T, -1)
+    o = bf16_round(ol.attention(q, kc, vc, wl["ctx"], c["window"], tree)).reshape(T, -1)
     x_mid = bf16_round(x + o @ Wn["w_o"].T)
     h = bf16_round(ol.rmsnorm(x_mid, Wn["ffn_norm_w"]))
     dev = W["w_router"].device

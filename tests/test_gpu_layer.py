@@ -203,165 +203,78 @@ def test_bounded_wait_reports_timeout_and_recovers(cuda_lib):
     H.compare_single(g, r, 4, 30)
 
 
-# ------------------------------------------------------------------ stacks
+# ------------------------------------------------------------ token trees
 
-def _stack_gpu(binding, work, T, ctx):
-    cfgs, Ws = work["cfgs"], work["Ws"]
-    L = len(Ws)
-    layers = []
-    max_ctx = work["caches"][0][0].shape[0]
-    for l in range(L):
-        flags = (binding.MK_FIRST_LAYER if l == 0 else 0) | (binding.MK_FUSE_NEXT_QKV if l + 1 < L else 0)
-        layers.append(H.make_layer(binding, cfgs[l], Ws[l], flags, max_ctx,
-                                   next_W=Ws[l + 1] if l + 1 < L else None))
-    stack = binding.mk_stack_create(layers)
-    kcs = [c[0].clone() for c in work["caches"]]
-    vcs = [c[1].clone() for c in work["caches"]]
-    x_in = work["x_in"][:T].contiguous()
-    x_out = torch.zeros_like(x_in)
-    moe = work["wl"]["ffn"] == "moe"
-    k = work["wl"].get("top_k", 1)
-    idx = torch.full((L, T, k), -1, dtype=torch.int32, device="cuda") if moe else None
-    io = binding.make_stack_io(T, ctx, x_in, x_out, kcs, vcs, topk_idx_out=idx)
-    binding.mk_stack_step(stack, io)
-    torch.cuda.synchronize()
-    st = binding.mk_stack_status(stack)
-    binding.mk_stack_destroy(stack)
-    for lay in layers:
-        binding.mk_layer_destroy(lay)
-    return dict(status=st, x_out=x_out.cpu(), k=[t.cpu() for t in kcs], v=[t.cpu() for t in vcs],
-                idx=idx.cpu().numpy() if moe else None)
+# 16 verify tokens as a tree (parent indices, -1 = a root after the prefix):
+# three branches of different depths, siblings at several levels.
+TREE_PARENTS = [-1, 0, 0, 0, 1, 1, 2, 4, 4, 5, 6, 7, 3, 12, 9, 13]
 
 
-def _router_input(cfg, W, x, kc, vc, ctx, q, first):
-    """h of one layer (the attention half of the oracle layer)."""
-    from oracle.numerics import bf16_round
-    T = x.shape[0]
-    kc, vc = kc.copy(), vc.copy()
-    if first:
-        q, kn, vn = ol.qkv_project(x, W["attn_norm_w"], W["w_qkv"], cfg["n_q_heads"],
-                                   cfg["n_kv_heads"], cfg["head_dim"])
-        kc[ctx:ctx + T], vc[ctx:ctx + T] = kn, vn
-    q = np.asarray(q).reshape(T, cfg["n_q_heads"], cfg["head_dim"])
-    o = bf16_round(ol.attention(q, kc, vc, ctx, cfg["window"])).reshape(T, -1)
-    x_mid = bf16_round(x + o @ W["w_o"].T)
-    return bf16_round(ol.rmsnorm(x_mid, W["ffn_norm_w"]))
+def tree_masks(parents):
+    m = []
+    for i, p in enumerate(parents):
+        m.append((1 << i) | (m[p] if p >= 0 else 0))
+    return m
 
 
-def _stack_oracle(work, T, ctx, enforce_margin):
-    """The oracle stack, redrawing each MoE layer's router (in layer order)
-    until the k-th/(k+1)-th logit gap is >= 1e-2 for every token."""
-    cfgs = [oio.oracle_cfg(c) for c in work["cfgs"]]
-    Ws = work["Ws"]
-    L = len(Ws)
-    Wn = [oio.np_weights(W) for W in Ws]
-    x = oio.np64(work["x_in"][:T])
-    kcs = [oio.np64(c[0]) for c in work["caches"]]
-    vcs = [oio.np64(c[1]) for c in work["caches"]]
-    q = None
-    per = []
-    for l in range(L):
-        nxt = Wn[l + 1] if l + 1 < L else None
-        if enforce_margin and cfgs[l]["ffn"] == "moe":
-            h = _router_input(cfgs[l], Wn[l], x, kcs[l], vcs[l], ctx, q, l == 0)
-            for draw in range(400):
-                wr = synth.router_weight(work["wl"], work["seed"], l, draw, Ws[l]["w_router"].device)
-                logits, _, _ = ol.router(h, oio.np64(wr), cfgs[l]["top_k"])
-                if np.all(oio.router_margin(logits, cfgs[l]["top_k"]) >= oio.MARGIN):
-                    Ws[l]["w_router"] = wr
-                    Wn[l]["w_router"] = oio.np64(wr)
-                    break
-            else:
-                raise RuntimeError("no router draw met the margin")
-        r = ol.layer_forward(cfgs[l], Wn[l], x, kcs[l], vcs[l], ctx, q_in=q,
-                             first_layer=(l == 0), next_W=nxt,
-                             next_k_cache=kcs[l + 1] if nxt else None,
-                             next_v_cache=vcs[l + 1] if nxt else None)
-        kcs[l], vcs[l] = r["k_cache"], r["v_cache"]
-        if nxt is not None:
-            kcs[l + 1], vcs[l + 1] = r["next_k_cache"], r["next_v_cache"]
-            q = r["q_next"]
-        x = r["x_out"]
-        per.append((r.get("idx"), r.get("logits")))
-    return dict(x_out=x, k=kcs, v=vcs, idx=[p[0] for p in per], logits=[p[1] for p in per])
+def _tree_single(binding, name, dev, T, ctx, tree, flips=False):
+    work, Wn = H.prepare(name, dev, T=T, ctx=ctx, enforce=False)
+    c = work["cfgs"][0]
+    # margin on the tree's router input (the oracle decides)
+    if c["ffn"] == "moe":
+        Wn, _ = oio.enforce_margin_single(work, tree=tree)
+    g = H.run_single_layer(binding, work, tree_mask=tree)
+    r = H.oracle_single_layer(work, Wn=Wn, tree=tree)
+    extra = 3.0 * oio.flip_tolerance_fast(c, Wn, r)[:, None] if flips else 0.0
+    return H.compare_single(g, r, T, ctx, moe=c["ffn"] == "moe", x_extra=extra)
 
 
-def _chained_single_layers(binding, work, T, ctx):
-    """The same chain run as separate mk_decode_step calls (x, q and the
-    next-layer K/V rows handed over on the device)."""
-    cfgs, Ws = work["cfgs"], work["Ws"]
-    L = len(Ws)
-    max_ctx = work["caches"][0][0].shape[0]
-    kcs = [c[0].clone() for c in work["caches"]]
-    vcs = [c[1].clone() for c in work["caches"]]
-    x = work["x_in"][:T].contiguous()
-    q = None
-    Hqd = cfgs[0]["n_q_heads"] * cfgs[0]["head_dim"]
-    for l in range(L):
-        fuse = l + 1 < L
-        flags = (binding.MK_FIRST_LAYER if l == 0 else 0) | (binding.MK_FUSE_NEXT_QKV if fuse else 0)
-        lay = H.make_layer(binding, cfgs[l], Ws[l], flags, max_ctx, next_W=Ws[l + 1] if fuse else None)
-        x_out = torch.zeros_like(x)
-        q_out = torch.zeros((T, Hqd), dtype=torch.bfloat16, device="cuda") if fuse else None
-        io = binding.make_step_io(T, ctx, x, x_out, kcs[l], vcs[l], q_in=q,
-                                  next_k_cache=kcs[l + 1] if fuse else None,
-                                  next_v_cache=vcs[l + 1] if fuse else None, q_out=q_out)
-        binding.mk_decode_step(lay, io)
+def test_tree_mask_of_the_chain_is_the_default(cuda_lib):
+    """The causal chain passed as an explicit tree gives the same bits as no
+    mask."""
+    work, _ = H.prepare("swa_layer", "cuda", ctx=3000, enforce=False)
+    a = H.run_single_layer(cuda_lib, work)
+    b = H.run_single_layer(cuda_lib, work, tree_mask=tree_masks(list(range(-1, 15))))
+    for key in ("x_out", "k_cache", "v_cache"):
+        assert torch.equal(a[key], b[key]), key
+
+
+def test_tree_verification_swa_layer(cuda_lib):
+    """Token-tree verification at the full shapes: 16 tokens in a tree, context
+    8192, window 2048, against the oracle's tree attention."""
+    _tree_single(cuda_lib, "swa_layer", "cuda", 16, 8192, tree_masks(TREE_PARENTS))
+
+
+def test_tree_verification_tiny_short_window(cuda_lib):
+    """A tree whose depth reaches past a short window (window 4): ancestors more
+    than 3 levels up are cut off like prefix positions."""
+    work_parents = [-1, 0, 1, 2, 3, 4, 1, 6]       # a chain of depth 5 and a side branch
+    wl = dict(synth.WORKLOADS["tiny_layer"], window=4)
+    work, _ = H.prepare(wl, "host", T=8, ctx=30, enforce=False)
+    Wn, _ = oio.enforce_margin_single(work, tree=tree_masks(work_parents))
+    g = H.run_single_layer(cuda_lib, work, tree_mask=tree_masks(work_parents))
+    r = H.oracle_single_layer(work, Wn=Wn, tree=tree_masks(work_parents))
+    extra = 3.0 * oio.flip_tolerance_fast(work["cfgs"][0], Wn, r)[:, None]
+    H.compare_single(g, r, 8, 30, x_extra=extra)
+
+
+def test_tree_masks_that_are_not_trees_are_refused(cuda_lib):
+    work, _ = H.prepare("tiny_layer", "host", T=4, ctx=30, enforce=False)
+    c = work["cfgs"][0]
+    kc, vc = (t.clone() for t in work["caches"][0])
+    layer = H.make_layer(cuda_lib, c, work["Ws"][0], cuda_lib.MK_FIRST_LAYER, kc.shape[0])
+    x = work["x_in"][:4].contiguous()
+    y = torch.zeros_like(x)
+    bad = [[1, 3, 5, 3],       # token 3 misses itself
+           [1, 3, 7, 0x18],    # token 3 holds a later token (bit 4)
+           [1, 3, 6, 13],      # token 2 lists 1 but not 1's ancestor 0
+           [3, 3, 7, 15]]      # token 0 holds token 1
+    try:
+        for m in bad:
+            with pytest.raises(cuda_lib.MkError) as e:
+                cuda_lib.mk_decode_step(layer, cuda_lib.make_step_io(4, 30, x, y, kc, vc, tree_mask=m))
+            assert e.value.status == 1, m
         torch.cuda.synchronize()
-        assert binding.mk_layer_status(lay) == 0
-        binding.mk_layer_destroy(lay)
-        x, q = x_out, q_out
-    return dict(x_out=x.cpu(), k=[t.cpu() for t in kcs], v=[t.cpu() for t in vcs])
-
-
-def _check_stack(binding, work, T, ctx, moe):
-    """(1) the PDL-chained stack equals the same layers launched one by one,
-    bit for bit; (2) against the oracle: layer 0's router indices bit-exact,
-    every later layer's choice a valid top-k of the oracle's logits (within
-    5e-2 of the k-th logit -- later layers see inputs that differ by the
-    rounding of the layers before), first-layer K/V rows within the contract,
-    and the final hidden state with cosine >= 0.9995.  (Rounding differences
-    compound over layers, so the per-element bound is checked per layer -- the
-    single-layer tests -- and not on the output of the chain.)"""
-    r = _stack_oracle(work, T, ctx, enforce_margin=moe)
-    g = _stack_gpu(binding, work, T, ctx)
-    c = _chained_single_layers(binding, work, T, ctx)
-    assert g["status"] == 0
-    assert torch.equal(g["x_out"], c["x_out"])
-    for l in range(len(r["k"])):
-        assert torch.equal(g["k"][l], c["k"][l]) and torch.equal(g["v"][l], c["v"][l]), l
-    if moe:
-        assert np.array_equal(np.sort(g["idx"][0], axis=1), np.sort(r["idx"][0], axis=1)), "layer 0"
-        for l in range(1, len(r["idx"])):
-            lg = r["logits"][l].astype(np.float64)
-            kth = -np.sort(-lg, axis=1)[:, work["wl"]["top_k"] - 1]
-            chosen = np.take_along_axis(lg, g["idx"][l].astype(np.int64), axis=1)
-            assert np.all(chosen >= kth[:, None] - 5e-2), "layer %d router not a valid top-k" % l
-            assert all(len(set(row.tolist())) == len(row) for row in g["idx"][l])
-    H.assert_close("k rows layer 0", g["k"][0][ctx:ctx + T].double().numpy(), r["k"][0][ctx:ctx + T])
-    H.assert_close("v rows layer 0", g["v"][0][ctx:ctx + T].double().numpy(), r["v"][0][ctx:ctx + T])
-    m = H.metrics(g["x_out"].double().numpy(), r["x_out"])
-    assert m["cos"] >= H.COS_TOL, m
-
-
-def test_dense_draft_stack(cuda_lib):
-    """5 dense GQA layers chained with programmatic dependent launch."""
-    work = synth.make_workload("dense_draft_stack", device="cuda")
-    _check_stack(cuda_lib, work, work["wl"]["T"], work["wl"]["ctx"], moe=False)
-
-
-def test_moe_stack_first_layers(cuda_lib):
-    """The first 4 layers of the 62-layer MoE stack (3 sliding-window, 1
-    global), context 16384, PDL-chained, router margin enforced per layer."""
-    work = synth.make_workload("moe_stack", device="cuda", layers=4)
-    _check_stack(cuda_lib, work, work["wl"]["T"], work["wl"]["ctx"], moe=True)
-
-
-def test_tiny_stack_mixed_windows(cuda_lib):
-    wl = dict(synth.WORKLOADS["tiny_layer"], layers=3, T=8, ctx=90)
-    work = synth.make_workload(wl, device="cpu")
-    for l, win in enumerate((32, 0, 16)):
-        work["cfgs"][l] = dict(work["cfgs"][l], window=win)
-    for key in ("Ws", "caches", "x_in"):
-        work[key] = H.to_device(work[key], "cuda")
-    _check_stack(cuda_lib, work, 8, 90, moe=True)
+        assert cuda_lib.mk_layer_status(layer) == 0
+    finally:
+        cuda_lib.mk_layer_destroy(layer)
