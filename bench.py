@@ -196,7 +196,7 @@ def algorithmic_bytes(c, T, ctx, n_experts_touched, first, fuse):
     return b
 
 
-def build_layers(B, work, prefetch_experts=None):
+def build_layers(B, work, prefetch_experts=None, prefetch_next_kv=False):
     cfgs, Ws = work["cfgs"], work["Ws"]
     L = len(Ws)
     max_ctx = work["caches"][0][0].shape[0]
@@ -204,6 +204,8 @@ def build_layers(B, work, prefetch_experts=None):
     for l in range(L):
         fuse = l + 1 < L or (L == 1 and work["next"] is not None)
         flags = (B.MK_FIRST_LAYER if l == 0 else 0) | (B.MK_FUSE_NEXT_QKV if fuse else 0)
+        if prefetch_next_kv and l + 1 < L:
+            flags |= B.MK_PREFETCH_NEXT_KV
         cfg = B.make_config(cfgs[l], flags=flags, max_ctx=max_ctx, prefetch_experts=prefetch_experts)
         wd = dict(Ws[l])
         nxt = Ws[l + 1] if l + 1 < L else work["next"]
@@ -216,11 +218,11 @@ def build_layers(B, work, prefetch_experts=None):
 class Runner:
     """Holds the device state of one replica and runs steps."""
 
-    def __init__(self, B, work, stream, prefetch_experts=None):
+    def __init__(self, B, work, stream, prefetch_experts=None, prefetch_next_kv=False):
         self.B, self.work, self.stream = B, work, stream
         wl = work["wl"]
         self.T, self.ctx = wl["T"], wl["ctx"]
-        self.layers = build_layers(B, work, prefetch_experts)
+        self.layers = build_layers(B, work, prefetch_experts, prefetch_next_kv)
         self.L = len(self.layers)
         self.stack = B.mk_stack_create(self.layers) if self.L > 1 else None
         self.kcs = [c[0] for c in work["caches"]]
@@ -412,6 +414,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="moe_stack")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="stacks: run only the first N layers (a short stack for profiling)")
     ap.add_argument("--impl", default="mk", choices=["mk", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
@@ -419,6 +423,9 @@ def main():
     ap.add_argument("--inputs", default="drift", choices=["drift", "independent", "fixed"],
                     help="MoE inputs between steps: x <- 0.9x + 0.436n (drift), a fresh "
                          "draw (independent) or the same x (fixed)")
+    ap.add_argument("--prefetch-next-kv", type=int, default=0,
+                    help="stacks: 1 = each layer fetches the next layer's old KV rows into L2 "
+                         "during its last weight phases (MK_PREFETCH_NEXT_KV)")
     ap.add_argument("--prefetch-experts", type=int, default=None,
                     help="MoE: experts of the previous step prefetched into L2 (default 0: "
                          "off, measured faster on these inputs)")
@@ -438,9 +445,11 @@ def main():
     torch.cuda.set_device(local_rank)
     from moe_decode_layer_persistent_gb300 import binding as B
     # each replica draws its own inputs (seed offset by rank)
-    work = synth.make_workload(args.workload, device="cuda", seed=replica_seed(args.workload, rank))
+    work = synth.make_workload(args.workload, device="cuda", seed=replica_seed(args.workload, rank),
+                               layers=args.layers)
     stream = torch.cuda.Stream()
-    R = Runner(B, work, stream, prefetch_experts=args.prefetch_experts)
+    R = Runner(B, work, stream, prefetch_experts=args.prefetch_experts,
+               prefetch_next_kv=bool(args.prefetch_next_kv))
     wl = work["wl"]
     single = R.L == 1
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
@@ -509,6 +518,7 @@ def main():
         "vs_baseline": None, "dtype": "bf16 + nvfp4 (fp32 accumulate)", "data": "synthetic",
         "config": {"workload": args.workload, "layers": R.L, "T": R.T, "ctx": R.ctx,
                    "hidden": wl["hidden"], "ffn": wl["ffn"],
+                   "prefetch_next_kv": bool(args.prefetch_next_kv) and R.L > 1,
                    "l2": "flushed between steps (512 MB write)" if single else
                          "inputs larger than L2 (%.1f GB read per step)" % (sum(alg) / 1e9),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
