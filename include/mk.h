@@ -68,7 +68,8 @@ typedef enum {
 #define MK_TOPK_RENORM   0x4u  /* combine weights renormalised over the top-k    */
 #define MK_PREFETCH_NEXT_KV 0x8u /* in a stack (mk_stack_step), fetch the next
                                     layer's old KV rows -- those its verify tokens
-                                    will see -- into L2 while this layer runs its
+                                    will see, when K and V together are at most
+                                    16 MB -- into L2 while this layer runs its
                                     last weight phases (page "Muse Spark Open:
                                     1,109 Tokens a Second ...", section "What the
                                     5.9 ms is still spent on": the next layer's

@@ -550,13 +550,20 @@ mk_status mk_stack_step(mk_stack* S, const mk_stack_io* io, void* stream) {
     mk_status st = fill_step(L, &s, params[l]);
     if (st != MK_OK) return st;
     if ((L->cfg.flags & MK_PREFETCH_NEXT_KV) && l + 1 < n) {
-      // the rows [lo, ctx) the next layer's verify tokens will see
+      // the rows [lo, ctx) the next layer's verify tokens will see, when K and
+      // V together stay within kNextKvMax (a sliding-window layer's 2 x 4 MB;
+      // a long global context would crowd the L2 that holds this layer's
+      // prefetched unpooler and next-QKV weights)
+      constexpr int64_t kNextKvMax = 16ll << 20;
       const mk_layer_config& nc = S->layers[l + 1]->cfg;
       const int64_t lo = nc.window ? std::max(0, io->ctx_len - nc.window + 1) : 0;
       const int64_t row = static_cast<int64_t>(nc.n_kv_heads) * nc.head_dim * 2;
-      params[l].nkv[0] = static_cast<const uint8_t*>(io->k_caches[l + 1]) + lo * row;
-      params[l].nkv[1] = static_cast<const uint8_t*>(io->v_caches[l + 1]) + lo * row;
-      params[l].nkv_bytes = static_cast<uint64_t>(io->ctx_len - lo) * row;
+      const int64_t bytes = (io->ctx_len - lo) * row;
+      if (2 * bytes <= kNextKvMax) {
+        params[l].nkv[0] = static_cast<const uint8_t*>(io->k_caches[l + 1]) + lo * row;
+        params[l].nkv[1] = static_cast<const uint8_t*>(io->v_caches[l + 1]) + lo * row;
+        params[l].nkv_bytes = static_cast<uint64_t>(bytes);
+      }
     }
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -72,8 +72,8 @@ struct Misc {
   int slots[kMaxT * kMaxK];        // slot (t*k + r) grouped by expert
   float rnorm[kMaxT];              // stager: RMSNorm factors of the phase input
   float srow_st[kMaxT];            // stager: row scales of p (its share of the p image)
+  float srow_b[kMaxT];             // warp 7: row scales of the expert image it builds
   float srow_ep[kMaxT * kMaxK];    // epilogue: NVFP4 row scales of the phase input
-  float srow_q[kMaxT];             // epilogue: row scales of the rows it quantises into an image
   float red[4][kMaxT];             // epilogue cross-warp reductions
   uint32_t comb_local[kMaxT][16];  // epilogue: this CTA's z contributions per (token, tile)
   int done_pairs[kMaxT * 16];      // epilogue: (token, tile) pairs this CTA completes
@@ -967,6 +967,56 @@ MK_DEV void topk_token(const LayerParams& P, int t) {
   }
 }
 
+// NVFP4 operand image (codes in K-blocks of 2048 B, then the scale chunks) of
+// `rows` bf16 rows of K inputs, by `nthr` threads (this one: `tid`): image
+// row i is the row at src + off(i), with row scale srow[i] (shared memory).
+// The codes and scales go to `img` (global) and, when `sm` is given, to an
+// operand buffer in shared memory (codes at its start, scales at kBSfOff).
+// Each thread loads four 16-element blocks before quantising them, so that
+// four L2 round trips overlap.  The readers of `img` copy it with the async
+// proxy after acquiring the release that publishes it, behind a proxy fence
+// of their own.
+template <class Off>
+MK_DEV void quantize_image(uint8_t* img, uint8_t* sm, int rows, int K, const float* srow,
+                           const __nv_bfloat16* src, Off off, int tid, int nthr) {
+  const int nblk = K / 16;
+  const int total = rows * nblk;
+  OperandSink sink{img, img + ((K + 255) / 256) * 2048, 0};
+  OperandSink sink_s{sm, sm + kBSfOff, 0};
+  for (int i0 = tid; i0 < total; i0 += 4 * nthr) {
+    uint4 r[4][2];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int i = i0 + q * nthr;
+      if (i < total) {
+        const uint4* p = reinterpret_cast<const uint4*>(src + off(i / nblk) + (i % nblk) * 16);
+        r[q][0] = __ldcg(p);
+        r[q][1] = __ldcg(p + 1);
+      }
+    }
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {
+      const int i = i0 + q * nthr;
+      if (i >= total) break;
+      // select the block's registers (no dynamically indexed array)
+      const uint4 c0 = q == 0 ? r[0][0] : q == 1 ? r[1][0] : q == 2 ? r[2][0] : r[3][0];
+      const uint4 c1 = q == 0 ? r[0][1] : q == 1 ? r[1][1] : q == 2 ? r[2][1] : r[3][1];
+      const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+      float x[16];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        x[2 * k] = __uint_as_float(w[k] << 16);
+        x[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+      }
+      uint32_t w0, w1, sb;
+      quantize_block16(x, srow[i / nblk], w0, w1, sb);
+      sink.r = sink_s.r = static_cast<uint32_t>(i / nblk);
+      if (img) sink.put(i % nblk, w0, w1, sb);
+      if (sm) sink_s.put(i % nblk, w0, w1, sb);
+    }
+  }
+}
+
 // NVFP4 row scale of p's row t (amax over the pooler tiles' partials).
 MK_DEV float p_row_scale(const LayerParams& P, int t) {
   float a = 0.f;
@@ -992,6 +1042,40 @@ MK_DEV void p_image_share(const LayerParams& P, const Smem& S, int tid) {
     quantize_block16(x, m->srow_st[t], w0, w1, sb);
     sink.r = static_cast<uint32_t>(t);
     sink.put(b, w0, w1, sb);
+  }
+}
+
+// Warp 7 (MoE): once the routing is known, the SwiGLU images of the active
+// experts i = blockIdx.x, blockIdx.x + grid, ... (at most one per CTA at the
+// full shapes): wait until all of the expert's gate/up tiles are counted in,
+// compute the NVFP4 row scales of its rows (amax over the tiles' partials),
+// quantise the rows once into the expert's image and release it to the down
+// units of every CTA.
+MK_DEV void build_expert_images(const LayerParams& P, const Smem& S, uint32_t epoch) {
+  Misc* m = S.m;
+  const int lane = lane_id();
+  if (!wait_bar(P, S, &m->route_ready, 0, ERR_TIMEOUT_ROUTE)) return;
+  for (int i = blockIdx.x; i < m->n_act; i += P.grid) {
+    const int e = m->act[i];
+    int ok = 1;
+    if (lane == 0) ok = flag_wait(P, S, P.exp_sync + e, static_cast<uint32_t>(P.I / 128), ERR_TIMEOUT_DATA) ? 1 : 0;
+    if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+    __syncwarp();  // the lanes' loads below follow lane 0's acquire
+    const int n = m->off[e + 1] - m->off[e];
+    const int* sl = m->slots + m->off[e];
+    if (lane < n) {
+      float a = 0.f;
+      for (int j = 0; j < P.I / 128; ++j) a = fmaxf(a, __ldcg(P.aamax + sl[lane] * (P.I / 128) + j));
+      const float sr = a > 0.f ? __fdiv_rn(a, 2688.0f) : 1.0f;
+      P.srow_a[sl[lane]] = sr;
+      m->srow_b[lane] = sr;
+    }
+    __syncwarp();
+    const int ld = P.I;
+    quantize_image(P.aq_img + static_cast<size_t>(e) * image_bytes(P.I), nullptr, n, P.I, m->srow_b, P.a_buf,
+                   [sl, ld](int r) { return static_cast<size_t>(sl[r]) * ld; }, lane, 32);
+    __syncwarp();  // every lane's image and scale writes precede lane 0's release
+    if (lane == 0) st_release(P.exp_sync + kMaxE + e, epoch + 1u);
   }
 }
 
@@ -1028,7 +1112,9 @@ MK_DEV bool stage_expert_phase(const LayerParams& P, const Smem& S, int ph, uint
     const Unit U = make_unit(P, S, ph, u);
     const uint32_t b = ucount & 1;
     const uint64_t w0 = tnow(P);
-    if (!gu && !group_flag_wait(P, S, P.exp_sync + kMaxE + U.expert, epoch + 1u, tid == 0, kBarStage, 64, 0))
+    // down: the expert's SwiGLU image (built by warp 7 of one CTA)
+    if (!gu && holds[b] != U.expert &&
+        !group_flag_wait(P, S, P.exp_sync + kMaxE + U.expert, epoch + 1u, tid == 0, kBarStage, 64, 0))
       return false;
     if (!group_mbar_wait(P, S, &m->bempty[b], b_ph[b] ^ 1, ERR_TIMEOUT_B, tid == 0, kBarStage, 64, 0))
       return false;
@@ -1299,51 +1385,6 @@ MK_DEV float epi_reduce16(const Smem& S, float (&v)[kMaxT], int et) {
   return r;
 }
 
-// NVFP4 operand image (codes in K-blocks of 2048 B, then the scale chunks) of
-// `rows` bf16 rows of K inputs, by the 128 epilogue threads: image row i is
-// the row at src + off(i), with row scale srow[i] (shared memory).  Each
-// thread loads four 16-element blocks before quantising them, so that four
-// L2 round trips overlap.
-template <class Off>
-MK_DEV void quantize_image(uint8_t* img, int rows, int K, const float* srow,
-                           const __nv_bfloat16* src, Off off, int et) {
-  const int nblk = K / 16;
-  const int total = rows * nblk;
-  OperandSink sink{img, img + ((K + 255) / 256) * 2048, 0};
-  for (int i0 = et; i0 < total; i0 += 4 * 128) {
-    uint4 r[4][2];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int i = i0 + q * 128;
-      if (i < total) {
-        const uint4* p = reinterpret_cast<const uint4*>(src + off(i / nblk) + (i % nblk) * 16);
-        r[q][0] = __ldcg(p);
-        r[q][1] = __ldcg(p + 1);
-      }
-    }
-#pragma unroll 1
-    for (int q = 0; q < 4; ++q) {
-      const int i = i0 + q * 128;
-      if (i >= total) break;
-      // select the block's registers (no dynamically indexed array)
-      const uint4 c0 = q == 0 ? r[0][0] : q == 1 ? r[1][0] : q == 2 ? r[2][0] : r[3][0];
-      const uint4 c1 = q == 0 ? r[0][1] : q == 1 ? r[1][1] : q == 2 ? r[2][1] : r[3][1];
-      const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-      float x[16];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        x[2 * k] = __uint_as_float(w[k] << 16);
-        x[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
-      }
-      uint32_t w0, w1, sb;
-      quantize_block16(x, srow[i / nblk], w0, w1, sb);
-      sink.r = static_cast<uint32_t>(i / nblk);
-      sink.put(i % nblk, w0, w1, sb);
-    }
-  }
-  // (the readers' bulk copies follow their acquire of the release that
-  // publishes the image, and a proxy fence of their own)
-}
 
 
 // Final values of one 128-row tile of a bf16 phase: acc[j][t] for the row
@@ -1495,33 +1536,11 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
       const float r = epi_reduce16_mask<true>(S, am, et, tmask);
       if (et < kMaxT && ((tmask >> et) & 1u))
         P.aamax[sl[__popc(tmask & ((1u << et) - 1u))] * (P.I / 128) + U.tile] = r;
-      // the expert's last finished gate/up tile computes the NVFP4 row scales
-      // of its SwiGLU rows, quantises the rows once into the expert's image
-      // and releases it to the down units
+      // this gate/up tile of the expert is written: count it in (no reply
+      // waited for; warp 7 of one CTA builds the expert's image once all of
+      // its tiles are in)
       epi_sync();
-      if (et == 0) {
-        const uint32_t old = atom_add_acq_rel(P.exp_sync + e, 1u);
-        const bool last = old == static_cast<uint32_t>(P.I / 128 - 1);
-        if (last) P.exp_sync[e] = 0;  // this launch's arrivals are all in
-        m->flag = last;
-      }
-      epi_sync();
-      if (m->flag) {
-        if (et < n) {
-          const int s = sl[et];
-          float a = 0.f;
-          for (int jj = 0; jj < P.I / 128; ++jj) a = fmaxf(a, __ldcg(P.aamax + s * (P.I / 128) + jj));
-          const float sr = a > 0.f ? __fdiv_rn(a, 2688.0f) : 1.0f;
-          P.srow_a[s] = sr;
-          m->srow_q[et] = sr;
-        }
-        epi_sync();
-        const int ld = P.I;
-        quantize_image(P.aq_img + static_cast<size_t>(e) * image_bytes(P.I), n, P.I, m->srow_q, P.a_buf,
-                       [sl, ld](int i) { return static_cast<size_t>(sl[i]) * ld; }, et);
-        epi_sync();
-        if (et == 0) st_release(P.exp_sync + kMaxE + e, m->epoch + 1u);
-      }
+      if (et == 0) red_release_add(P.exp_sync + e, 1u);
     } else {
       const float td = ts0;
       for (int i = 0; i < n; ++i) {
@@ -2079,12 +2098,17 @@ MK_DEV void run_epilogue(const LayerParams& P, const Smem& S, uint32_t epoch) {
   }
   // CTA 0 advances the epoch once every CTA has finished this launch.
   if (ok && blockIdx.x == 0) {
-    if (epi_wait(P, S, final_barrier(P), target, et) && et == 0) {
-      // every CTA has claimed its last unit: the counters start the next
-      // launch at zero
-      for (int i = 0; i < PH_COUNT; ++i) P.sched[i] = 0;
-      __threadfence();
-      *P.epoch = epoch + 1u;
+    if (epi_wait(P, S, final_barrier(P), target, et)) {
+      // every CTA has claimed its last unit and counted in its last gate/up
+      // tile: the claim and per-expert counters start the next launch at zero
+      if (P.moe)
+        for (int i = et; i < P.E; i += 128) P.exp_sync[i] = 0;
+      epi_sync();
+      if (et == 0) {
+        for (int i = 0; i < PH_COUNT; ++i) P.sched[i] = 0;
+        __threadfence();
+        *P.epoch = epoch + 1u;
+      }
     }
   }
 }
@@ -2155,8 +2179,9 @@ __global__ void __launch_bounds__(kThreads, 1) mk_layer_kernel(const __grid_cons
       run_stager(P, S, epoch);
     } else if (warp >= 8) {
       run_epilogue(P, S, epoch);
-    } else if (warp == 7 && blockIdx.x == 0 && P.pf_n > 0) {
-      prefetch_bookkeeping(P, S, epoch);
+    } else if (warp == 7) {
+      if (blockIdx.x == 0 && P.pf_n > 0) prefetch_bookkeeping(P, S, epoch);
+      if (P.moe) build_expert_images(P, S, epoch);
     }
   }
   tc_fence_before();

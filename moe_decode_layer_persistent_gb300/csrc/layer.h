@@ -124,9 +124,9 @@ struct LayerParams {
   float* attn_part;         // [Hkv*chunks][64][d + 2]
   uint32_t* fix_ctr;        // fixup counters per (phase, tile)  [PH_COUNT][256]
   uint32_t* comb_ctr;       // combine counters [16][P/128]
-  uint32_t* exp_sync;       // MoE: [0, 256) finished gate/up tiles per expert (the
-                            // last one resets it), [256, 512) expert's SwiGLU rows
-                            // and their scales ready (epoch + 1)
+  uint32_t* exp_sync;       // MoE: [0, 256) finished gate/up tiles per expert (reset
+                            // by CTA 0 at the end of a launch), [256, 512) expert's
+                            // SwiGLU image and row scales ready (epoch + 1)
   float* srow_a;            // MoE: NVFP4 row scales of the SwiGLU rows [16*k]
   // MoE: the expert MMAs' token operands, NVFP4-quantised once per launch in
   // the layout of a shared-memory operand buffer (image_bytes(K) each: codes
