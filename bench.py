@@ -561,6 +561,9 @@ def main():
         line["expert_prefetch_14"] = var
         line["expert_prefetch_14"]["note"] = ("prefetch on; the headline runs with it off "
                                               "(prefetch_experts=0)")
+    if not args.no_extras:
+        # intra-GPU synchronisation costs (the pages measure the cross-GPU ones)
+        line["sync_ns"] = {m: round(B.mk_selftest_sync(m, 20000), 1) for m in B.SYNC_MODES}
     if not single and not args.no_extras and args.workload == "moe_stack":
         # config 2 per layer: one sliding-window layer, L2 flushed between steps
         sw = synth.make_workload("swa_layer", device="cuda", seed=replica_seed("swa_layer", rank))

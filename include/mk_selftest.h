@@ -28,6 +28,17 @@ mk_status mk_selftest_quantize(const void* x, int32_t rows, int32_t K, void* cod
 mk_status mk_selftest_mma(int32_t fp4, const void* a, const void* a_scales, const void* b,
                           const void* b_scales, int32_t K, float* out, void* stream);
 
+/* Intra-GPU synchronisation costs in ns (page "Muse Spark Open: 1,109 Tokens a
+ * Second ...", section "Three bills a kernel this big has to pay", measures
+ * the cross-GPU ones): mode 0, one hop of a flag between two CTAs on two SMs
+ * (st.release / ld.acquire polling); mode 1, one hop of a bf16 value that is
+ * its own signal (relaxed store, relaxed polling until the word holds the
+ * round's value); mode 2, one ld.acquire.gpu poll of a resident word; mode 3, one
+ * fence.acq_rel.gpu with nothing in flight.  `iters` rounds (1 .. 2^20);
+ * every poll is bounded (MK_ERR_TIMEOUT if one gives up).  Synchronous;
+ * allocates and frees its own 256 bytes. */
+mk_status mk_selftest_sync(int32_t mode, int32_t iters, double* ns_per_op);
+
 #ifdef __cplusplus
 }
 #endif

@@ -113,6 +113,9 @@ _lib_mk_selftest_mma = _sig("mk_selftest_mma", _c.c_int,
 
 _lib_mk_get_timestamps = _sig("mk_get_timestamps", _c.c_int, [_vp, _c.c_void_p, _c.c_size_t])
 
+_lib_mk_selftest_sync = _sig("mk_selftest_sync", _c.c_int,
+                             [_c.c_int32, _c.c_int32, _c.POINTER(_c.c_double)])
+
 _lib_mk_decode_step_noalloc = _sig("mk_decode_step_noalloc", _c.c_int,
                                    [_c.POINTER(mk_layer_config), _c.POINTER(mk_layer_weights),
                                     _c.POINTER(mk_step_io), _vp])
@@ -121,7 +124,7 @@ EXPORTED = ["mk_layer_create", "mk_decode_step", "mk_decode_step_noalloc", "mk_l
             "mk_layer_destroy", "mk_stack_create", "mk_stack_step", "mk_stack_status",
             "mk_stack_destroy", "mk_status_string", "mk_layer_get_info", "mk_get_timestamps",
             "mk_layer_prefetch_stats", "mk_stack_prefetch_stats",
-            "mk_selftest_quantize", "mk_selftest_mma"]
+            "mk_selftest_quantize", "mk_selftest_mma", "mk_selftest_sync"]
 
 
 def _ptr(t):
@@ -307,3 +310,14 @@ def mk_get_timestamps(layer, grid):
     buf = np.zeros((grid, 10, 16), dtype=np.uint64)
     _check("mk_get_timestamps", _lib_mk_get_timestamps(layer, buf.ctypes.data, buf.size))
     return buf
+
+
+SYNC_MODES = {"flag_hop": 0, "sentinel_hop": 1, "acquire_poll": 2, "fence": 3}
+
+
+def mk_selftest_sync(mode, iters=10000):
+    """ns per operation of an intra-GPU synchronisation primitive (see mk_selftest.h)."""
+    m = SYNC_MODES[mode] if isinstance(mode, str) else mode
+    out = _c.c_double()
+    _check("mk_selftest_sync", _lib_mk_selftest_sync(m, iters, _c.byref(out)))
+    return out.value

@@ -126,9 +126,105 @@ __global__ void __launch_bounds__(256, 1)
   if (warp == 1) tmem_dealloc(tbase, 256);
 }
 
+// Intra-GPU synchronisation costs (the synchronisation bill of page "Muse
+// Spark Open: 1,109 Tokens a Second ...", section "Three bills a kernel this
+// big has to pay", measured within one GPU).  modes 0/1: CTAs 0 and 1 of a
+// cooperative launch (one per SM) ping-pong `iters` rounds; CTA 0 times the
+// rounds with %globaltimer and reports half a round trip:
+//   0: a flag word: st.release.gpu of the round number, polled with
+//      ld.acquire.gpu;
+//   1: the data as the signal: each round's value (a bf16 number that
+//      differs from the previous round's) is written with a relaxed store and
+//      polled with relaxed loads until the word holds it -- no fence, no
+//      acquire.
+// mode 2: one ld.acquire.gpu poll of a resident word, back to back (CTA 0).
+// mode 3: one fence.acq_rel.gpu with no memory traffic in flight (CTA 0).
+// Every poll gives up after kPollLimit tries and sets *status.
+constexpr uint32_t kPollLimit = 1u << 20;
+
+MK_DEV uint16_t ld_relaxed_u16(const uint16_t* p) {
+  uint16_t v;
+  asm volatile("ld.relaxed.gpu.global.u16 %0, [%1];" : "=h"(v) : "l"(p) : "memory");
+  return v;
+}
+MK_DEV void st_relaxed_u16(uint16_t* p, uint16_t v) {
+  asm volatile("st.relaxed.gpu.global.u16 [%0], %1;" ::"l"(p), "h"(v) : "memory");
+}
+MK_DEV void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+__global__ void __launch_bounds__(32, 1)
+    k_selftest_sync(int mode, int iters, uint32_t* flags, uint16_t* slots, uint32_t* status,
+                    unsigned long long* ns) {
+  if (threadIdx.x != 0) return;
+  const int me = blockIdx.x;
+  uint64_t t0 = globaltimer();
+  if (mode == 0) {
+    for (int r = 1; r <= iters; ++r) {
+      // CTA 0 sends round r on flags[0] and waits for the echo on flags[1]
+      if (me == 0) st_release(flags, static_cast<uint32_t>(r));
+      const uint32_t* in = flags + (me == 0 ? 1 : 0);
+      uint32_t n = 0;
+      while (ld_acquire(in) != static_cast<uint32_t>(r)) {
+        if (++n == kPollLimit) { atomicExch(status, 1u); return; }
+      }
+      if (me == 1) st_release(flags + 1, static_cast<uint32_t>(r));
+    }
+  } else if (mode == 1) {
+    uint16_t* out = slots + me;
+    const uint16_t* in = slots + (me ^ 1);
+    for (int r = 1; r <= iters; ++r) {
+      const uint16_t val = static_cast<uint16_t>(0x3F80u + (r & 63));  // a bf16 number
+      if (me == 0) st_relaxed_u16(out, val);
+      uint32_t n = 0;
+      while (ld_relaxed_u16(in) != val) {
+        if (++n == kPollLimit) { atomicExch(status, 1u); return; }
+      }
+      if (me == 1) st_relaxed_u16(out, val);
+    }
+  } else if (mode == 2) {
+    if (me != 0) return;
+    uint32_t acc = 0;
+    for (int r = 0; r < iters; ++r) acc += ld_acquire(flags + 2);
+    if (acc == 0xFFFFFFFFu) flags[3] = acc;  // keeps the loads
+  } else {
+    if (me != 0) return;
+    for (int r = 0; r < iters; ++r) fence_acq_rel_gpu();
+  }
+  if (me == 0) *ns = globaltimer() - t0;
+}
+
 }  // namespace mk
 
 using namespace mk;
+
+extern "C" mk_status mk_selftest_sync(int32_t mode, int32_t iters, double* ns_per_op) {
+  if (!ns_per_op || mode < 0 || mode > 3 || iters < 1 || iters > (1 << 20)) return MK_ERR_INVALID_ARG;
+  uint8_t* buf = nullptr;
+  MK_CUDA_TRY(cudaMalloc(&buf, 256));
+  uint32_t* flags = reinterpret_cast<uint32_t*>(buf);
+  uint16_t* slots = reinterpret_cast<uint16_t*>(buf + 64);
+  uint32_t* status = reinterpret_cast<uint32_t*>(buf + 128);
+  unsigned long long* ns = reinterpret_cast<unsigned long long*>(buf + 192);
+  cudaError_t e = cudaMemset(buf, 0, 256);
+  // 150 KB of shared memory per CTA: the two CTAs land on different SMs
+  const int smem = 150 * 1024;
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_selftest_sync, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  void* args[] = {&mode, &iters, &flags, &slots, &status, &ns};
+  if (e == cudaSuccess)
+    e = cudaLaunchCooperativeKernel(reinterpret_cast<void*>(k_selftest_sync), dim3(2), dim3(32), args, smem, 0);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  unsigned long long h_ns = 0;
+  uint32_t h_status = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&h_ns, ns, sizeof(h_ns), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemcpy(&h_status, status, sizeof(h_status), cudaMemcpyDeviceToHost);
+  cudaFree(buf);
+  if (e != cudaSuccess) return MK_ERR_CUDA;
+  if (h_status) return MK_ERR_TIMEOUT;
+  // modes 0/1: a round is two hops
+  *ns_per_op = static_cast<double>(h_ns) / iters / (mode <= 1 ? 2.0 : 1.0);
+  return MK_OK;
+}
 
 extern "C" mk_status mk_selftest_quantize(const void* x, int32_t rows, int32_t K, void* codes,
                                           void* scales, float* s_row, void* stream) {

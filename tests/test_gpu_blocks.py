@@ -72,3 +72,14 @@ def test_mma_tile_nvfp4(cuda_lib, K, mode):
     want = B @ A.T
     got = out.cpu().double().numpy()
     assert np.allclose(got, want, rtol=1e-5, atol=1e-5 * np.abs(want).max())
+
+
+def test_sync_microbenchmark(cuda_lib):
+    """Intra-GPU synchronisation costs (one flag hop between two SMs, one hop
+    of a value that is its own signal, one acquire poll, one idle fence) are
+    measured without any poll giving up, and fall in a plausible range."""
+    got = {m: cuda_lib.mk_selftest_sync(m, 2000) for m in cuda_lib.SYNC_MODES}
+    for m, ns in got.items():
+        assert 1.0 < ns < 1e5, (m, ns)
+    assert got["acquire_poll"] < got["flag_hop"], got
+
