@@ -263,8 +263,9 @@ mk_status mk_layer_get_info(mk_layer* layer, mk_layer_info* info);
  * input dependency met, epilogue starts the phase's units);
  * row 9 starts with (kernel start, inputs ready, kernel end, this CTA's
  * router top-k start and its routing arrival -- CTAs 0..T-1 select one token
- * each -- and router logits complete, in the CTA that finished the last
- * router tile).  All values are of the last step; stamps of
+ * each --, router logits complete (in the CTA that finished the last router
+ * tile), p complete seen by this CTA's stagers, its share of the p image
+ * written).  All values are of the last step; stamps of
  * unused phases read 0.  Each CTA keeps them in shared memory and writes them
  * out when it exits, so that timing costs little.  Synchronous. */
 mk_status mk_get_timestamps(mk_layer* layer, uint64_t* host_buf, size_t n);

@@ -1017,27 +1017,46 @@ MK_DEV void quantize_image(uint8_t* img, uint8_t* sm, int rows, int K, const flo
   }
 }
 
+// The sum (in index order, from 0) or the maximum (from 0) of the n
+// per-tile partials p[j * stride], j < n.  The loads go out 32 at a time, so
+// that the partials of a 4096-wide row cost one L2 round trip, not one per
+// partial; the arithmetic is that of the plain loop.
+template <bool kMax>
+MK_DEV float reduce_partials(const float* p, int n, int stride) {
+  float acc = 0.f;
+  for (int j0 = 0; j0 < n; j0 += 32) {
+    float v[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) v[k] = j0 + k < n ? __ldcg(p + static_cast<size_t>(j0 + k) * stride) : 0.f;
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      if (j0 + k < n) acc = kMax ? fmaxf(acc, v[k]) : acc + v[k];
+  }
+  return acc;
+}
+
 // NVFP4 row scale of p's row t (amax over the pooler tiles' partials).
 MK_DEV float p_row_scale(const LayerParams& P, int t) {
-  float a = 0.f;
-  for (int j = 0; j < P.P / 128; ++j) a = fmaxf(a, __ldcg(P.pamax + j * kMaxT + t));
+  const float a = reduce_partials<true>(P.pamax + t, P.P / 128, kMaxT);
   return a > 0.f ? __fdiv_rn(a, 2688.0f) : 1.0f;
 }
 
-// This CTA's 1/grid share of the p image's 16-element blocks (T rows of P), by
-// the 64 stager threads: one block per thread at the full shapes.
-MK_DEV void p_image_share(const LayerParams& P, const Smem& S, int tid) {
+// Share `sharer` (of `nsh`) of the p image's 16-element blocks (T rows of P),
+// by the 64 stager threads: one block per thread at the full shapes.  The
+// block's values are in flight while the row scales are gathered.
+MK_DEV void p_image_share(const LayerParams& P, const Smem& S, int tid, int sharer, int nsh) {
   Misc* m = S.m;
+  const int nblk = P.P / 16, total = P.T * nblk;
+  const int per = (total + nsh - 1) / nsh;
+  const int lo = sharer * per, hi = min(total, lo + per);
+  float x[16];
+  if (lo + tid < hi) load_bf16x16_cg(P.p_buf + static_cast<size_t>((lo + tid) / nblk) * P.P + ((lo + tid) % nblk) * 16, x);
   if (tid < P.T) m->srow_st[tid] = p_row_scale(P, tid);
   stage_sync();
-  const int nblk = P.P / 16, total = P.T * nblk;
-  const int per = (total + P.grid - 1) / P.grid;
-  const int lo = static_cast<int>(blockIdx.x) * per, hi = min(total, lo + per);
   OperandSink sink{P.pq_img, P.pq_img + ((P.P + 255) / 256) * 2048, 0};
   for (int i = lo + tid; i < hi; i += 64) {
     const int t = i / nblk, b = i % nblk;
-    float x[16];
-    load_bf16x16_cg(P.p_buf + static_cast<size_t>(t) * P.P + b * 16, x);
+    if (i != lo + tid) load_bf16x16_cg(P.p_buf + static_cast<size_t>(t) * P.P + b * 16, x);
     uint32_t w0, w1, sb;
     quantize_block16(x, m->srow_st[t], w0, w1, sb);
     sink.r = static_cast<uint32_t>(t);
@@ -1064,8 +1083,7 @@ MK_DEV void build_expert_images(const LayerParams& P, const Smem& S, uint32_t ep
     const int n = m->off[e + 1] - m->off[e];
     const int* sl = m->slots + m->off[e];
     if (lane < n) {
-      float a = 0.f;
-      for (int j = 0; j < P.I / 128; ++j) a = fmaxf(a, __ldcg(P.aamax + sl[lane] * (P.I / 128) + j));
+      const float a = reduce_partials<true>(P.aamax + sl[lane] * (P.I / 128), P.I / 128, 1);
       const float sr = a > 0.f ? __fdiv_rn(a, 2688.0f) : 1.0f;
       P.srow_a[sl[lane]] = sr;
       m->srow_b[lane] = sr;
@@ -1190,8 +1208,13 @@ MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
     if (ph == PH_GU) {
       // the router top-k, one token per CTA: CTA t < T selects token t's
       // experts with its first stager warp once the logits are complete; the
-      // arrivals add up to grid (CTA 0 adds the CTAs without a token)
+      // arrivals add up to grid (CTA 0 adds the CTAs without a token).  The p
+      // image is quantised in shares by the other CTAs (by all when grid == T):
+      // a top-k CTA without a share arrives at once.
+      const int nsh = P.grid > P.T ? P.grid - P.T : P.grid;
+      const int sharer = static_cast<int>(blockIdx.x) - (P.grid - nsh);
       if (static_cast<int>(blockIdx.x) < P.T) {
+        if (sharer < 0 && tid == 0) red_release_add(P.bar_ctr + BAR_PQ, 1u);
         if (!group_flag_wait(P, S, P.misc_ctr + 3, epoch + 1u, tid == 0, kBarStage, 64, 0)) { ok = false; break; }
         if (warp == 0) {
           if (tid == 0) stamp(P, S, PH_COUNT, 3);
@@ -1205,10 +1228,16 @@ MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
         }
       }
       // once p is complete, this CTA's share of the p image
-      if (!group_flag_wait(P, S, P.misc_ctr + 2, epoch + 1u, tid == 0, kBarStage, 64, 0)) { ok = false; break; }
-      p_image_share(P, S, tid);
-      stage_sync();
-      if (tid == 0) red_release_add(P.bar_ctr + BAR_PQ, 1u);
+      if (sharer >= 0) {
+        if (!group_flag_wait(P, S, P.misc_ctr + 2, epoch + 1u, tid == 0, kBarStage, 64, 0)) { ok = false; break; }
+        if (tid == 0) stamp(P, S, PH_COUNT, 6);
+        p_image_share(P, S, tid, sharer, nsh);
+        stage_sync();
+        if (tid == 0) {
+          red_release_add(P.bar_ctr + BAR_PQ, 1u);
+          stamp(P, S, PH_COUNT, 7);
+        }
+      }
       // the expert weights depend only on the routing: publish it to the
       // producer before waiting for the rest of the p image
       if (!group_grid_wait(P, S, BAR_ROUTE, target, tid == 0, kBarStage, 64, 0)) { ok = false; break; }
@@ -1231,8 +1260,7 @@ MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
     if (ph == PH_RP || ph == PH_NQKV) {
       const float* ssq = ph == PH_RP ? P.ssq_mid : P.ssq_out;
       if (tid < P.T) {
-        float s = 0.f;
-        for (int j = 0; j < P.H / 128; ++j) s += __ldcg(ssq + j * kMaxT + tid);
+        const float s = reduce_partials<false>(ssq + tid, P.H / 128, kMaxT);
         m->rnorm[tid] = 1.0f / sqrtf(s / P.H + P.eps);
       }
     }
@@ -1384,8 +1412,6 @@ MK_DEV float epi_reduce16(const Smem& S, float (&v)[kMaxT], int et) {
   epi_sync();
   return r;
 }
-
-
 
 // Final values of one 128-row tile of a bf16 phase: acc[j][t] for the row
 // (feature) f of this thread.
