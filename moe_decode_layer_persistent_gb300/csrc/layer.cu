@@ -46,7 +46,10 @@ constexpr uint32_t kBSfOff = 16384;                          // scales inside a 
 constexpr uint32_t kLandOff = 16384;   // bf16 units: raw input rows (<= 16 KB), then the gain slice
 constexpr uint32_t kOffMisc = kOffB + 2 * kBBufBytes;
 constexpr uint32_t kOffTs = kOffMisc + 8192;                 // self-timing block
-constexpr uint32_t kSmemBytes = kOffTs + kTsPerCta * 8 + 1024;   // + alignment slack
+constexpr uint32_t kOffRes = (kOffTs + kTsPerCta * 8 + 127) & ~127u;  // epilogue: residual rows of a tile
+constexpr uint32_t kResBytes = kMaxT * 128 * 2;
+constexpr uint32_t kSmemBytes = kOffRes + kResBytes + 1024;   // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 struct Misc {
   uint64_t full[kStages];
@@ -92,6 +95,7 @@ struct Smem {
   MK_DEV uint8_t* a_tile(int s) const { return base + kOffA + s * kTileBytes; }
   MK_DEV uint8_t* sf(int s) const { return base + kOffSF + s * kSfBytes; }
   MK_DEV uint8_t* bbuf(int b) const { return base + kOffB + b * kBBufBytes; }
+  MK_DEV uint8_t* res() const { return base + kOffRes; }
 };
 
 // ------------------------------------------------------------ errors / waits
@@ -1413,10 +1417,40 @@ MK_DEV float epi_reduce16(const Smem& S, float (&v)[kMaxT], int et) {
   return r;
 }
 
+// 16-byte global -> shared copies (zero fill when !valid), completed in groups.
+MK_DEV void cp_async16(uint32_t dst, const void* src, bool valid) {
+  const int n = valid ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n)
+               : "memory");
+}
+MK_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+MK_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// The residual phases (o-proj, unpooler, dense down) add the layer input
+// x_in (o-proj) or x_mid to their output.
+MK_DEV bool residual_phase(int ph) { return ph == PH_O || ph == PH_UNPOOL || ph == PH_DOWN; }
+MK_DEV const __nv_bfloat16* residual_src(const LayerParams& P, int ph) { return ph == PH_O ? P.x_in : P.xmid; }
+// Asynchronous copy of a tile's residual rows (T rows of 128 columns from
+// U.row0) into the epilogue's staging area: two 16-byte chunks per thread,
+// rows >= T zero.  Issued by the last unit of a split-K tile before it reads
+// the partials, so that both round trips overlap; epi_bf16_final waits.
+MK_DEV void stage_residual(const LayerParams& P, const Smem& S, int ph, const Unit& U, int et) {
+  const __nv_bfloat16* res = residual_src(P, ph);
+  for (int c = et; c < kMaxT * 16; c += 128) {
+    const int t = c >> 4, col = U.row0 + (c & 15) * 8;
+    const bool valid = t < P.T && col < U.N;
+    cp_async16(smem_u32(S.res() + c * 16), res + (valid ? static_cast<size_t>(t) * P.H + col : 0), valid);
+  }
+  cp_async_commit();
+}
+
 // Final values of one 128-row tile of a bf16 phase: acc[j][t] for the row
 // (feature) f of this thread.
+// `staged`: the residual rows are in flight to the staging area
+// (stage_residual), else they are loaded here.
 MK_DEV void epi_bf16_final(const LayerParams& P, const Smem& S, int ph, const Unit& U, int et,
-                           float (&g)[kMaxT], float (&u)[kMaxT]) {
+                           float (&g)[kMaxT], float (&u)[kMaxT], bool staged) {
   const int f = U.row0 + et;
   const bool valid = f < U.N;
   switch (ph) {
@@ -1438,15 +1472,23 @@ MK_DEV void epi_bf16_final(const LayerParams& P, const Smem& S, int ph, const Un
     case PH_O:
     case PH_UNPOOL:
     case PH_DOWN: {  // residual: x = bf16(res + acc); sum-of-squares partial
-      const __nv_bfloat16* res = ph == PH_O ? P.x_in : P.xmid;
       __nv_bfloat16* dst = ph == PH_O ? P.xmid : P.x_out;
       // every residual load is issued before the first store: a load may not
       // move past a store that could alias it, so interleaving them would cost
       // one memory round trip per token
       float rv[kMaxT];
+      if (staged) {
+        cp_async_wait<0>();
+        epi_sync();  // every thread's chunks have landed
 #pragma unroll
-      for (int t = 0; t < kMaxT; ++t)
-        rv[t] = (valid && t < P.T) ? ld_bf(res + static_cast<size_t>(t) * P.H + f) : 0.f;
+        for (int t = 0; t < kMaxT; ++t)
+          rv[t] = valid ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(S.res() + t * 256)[et]) : 0.f;
+      } else {
+        const __nv_bfloat16* res = residual_src(P, ph);
+#pragma unroll
+        for (int t = 0; t < kMaxT; ++t)
+          rv[t] = (valid && t < P.T) ? ld_bf(res + static_cast<size_t>(t) * P.H + f) : 0.f;
+      }
       float sq[kMaxT];
 #pragma unroll
       for (int t = 0; t < kMaxT; ++t) {
@@ -1579,6 +1621,7 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
   }
 
   // bf16 phase: split-K partials + fix-up by the last arriving unit of a tile
+  bool staged = false;
   if (U.ksplit > 1) {
     // the o-proj overlaps the QKV phase (per head group), so it has its own
     float* part = ph == PH_O ? P.part_o : P.part;
@@ -1602,6 +1645,12 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
     }
     epi_sync();
     if (!m->flag) return true;
+    // the last unit of the tile: its residual loads go out with the first
+    // partials' loads
+    if (residual_phase(ph)) {
+      stage_residual(P, S, ph, U, et);
+      staged = true;
+    }
     for (int j = 0; j < U.pair; ++j) {
       float acc[kMaxT];
 #pragma unroll
@@ -1634,7 +1683,7 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
       for (int t = 0; t < kMaxT; ++t) (j ? u : g)[t] = acc[t];
     }
   }
-  epi_bf16_final(P, S, ph, U, et, g, u);
+  epi_bf16_final(P, S, ph, U, et, g, u, staged);
   if (ph == PH_QKV) {
     // this tile's q, k and v rows are final: count it in for its groups (a
     // counter that grows by grp_tiles per launch; no reply is waited for)
@@ -1690,15 +1739,6 @@ MK_DEV void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, u
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
 }
-MK_DEV void cp_async16(uint32_t dst, const void* src, bool valid) {
-  const int n = valid ? 16 : 0;
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n)
-               : "memory");
-}
-MK_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-MK_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
 MK_DEV uint32_t pack_bf16(float a, float b) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&v);
