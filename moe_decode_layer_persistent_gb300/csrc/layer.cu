@@ -48,7 +48,9 @@ constexpr uint32_t kOffMisc = kOffB + 2 * kBBufBytes;
 constexpr uint32_t kOffTs = kOffMisc + 8192;                 // self-timing block
 constexpr uint32_t kOffRes = (kOffTs + kTsPerCta * 8 + 127) & ~127u;  // epilogue: residual rows of a tile
 constexpr uint32_t kResBytes = kMaxT * 128 * 2;
-constexpr uint32_t kSmemBytes = kOffRes + kResBytes + 1024;   // + alignment slack
+constexpr uint32_t kOffTsc = kOffRes + kResBytes;            // epilogue: experts' NVFP4 tensor scales
+constexpr uint32_t kTscBytes = 3 * kMaxE * 4;
+constexpr uint32_t kSmemBytes = kOffTsc + kTscBytes + 1024;   // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 struct Misc {
@@ -96,6 +98,8 @@ struct Smem {
   MK_DEV uint8_t* sf(int s) const { return base + kOffSF + s * kSfBytes; }
   MK_DEV uint8_t* bbuf(int b) const { return base + kOffB + b * kBBufBytes; }
   MK_DEV uint8_t* res() const { return base + kOffRes; }
+  // tensor scales of the launch's active experts: [0] gate, [1] up, [2] down, by expert
+  MK_DEV float* tsc(int w) const { return reinterpret_cast<float*>(base + kOffTsc) + w * kMaxE; }
 };
 
 // ------------------------------------------------------------ errors / waits
@@ -1536,12 +1540,6 @@ MK_DEV void epi_bf16_final(const LayerParams& P, const Smem& S, int ph, const Un
 MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Unit& U,
                           uint32_t b, uint32_t& acc_ph_b, int et) {
   Misc* m = S.m;
-  // an expert unit's tensor scales, loaded while the accumulator is awaited
-  float ts0 = 0.f, ts1 = 0.f;
-  if (U.fp4) {
-    ts0 = __ldg(ph == PH_GU ? P.ts_gate + U.expert : P.ts_down + U.expert);
-    if (ph == PH_GU) ts1 = __ldg(P.ts_up + U.expert);
-  }
   const uint64_t w0 = tnow(P);
   if (!group_mbar_wait(P, S, &m->accfull[b], acc_ph_b, ERR_TIMEOUT_ACC, et == 0, kBarEpi, 128, 1))
     return false;
@@ -1577,7 +1575,7 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
     if (ph == PH_GU) {
       // Accumulator column t is token t (the p image holds every token).  The
       // expert's slots, ascending, name its tokens in ascending order.
-      const float tg = ts0, tu = ts1;
+      const float tg = S.tsc(0)[e], tu = S.tsc(1)[e];
       const int* sl = m->slots + m->off[e];
       float am[kMaxT];
       uint32_t tmask = 0;
@@ -1610,7 +1608,7 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
       epi_sync();
       if (et == 0) red_release_add(P.exp_sync + e, 1u);
     } else {
-      const float td = ts0;
+      const float td = S.tsc(2)[e];
       for (int i = 0; i < n; ++i) {
         const int s = m->slots[m->off[e] + i];
         P.z_buf[static_cast<size_t>(s) * P.P + f] = to_bf(g[i] * m->srow_ep[s] * td);
@@ -2130,6 +2128,14 @@ MK_DEV void run_epilogue(const LayerParams& P, const Smem& S, uint32_t epoch) {
       // p complete: its row scales from the amax partials
       if (!(ok = group_flag_wait(P, S, P.misc_ctr + 2, epoch + 1u, et == 0, kBarEpi, 128, 1))) break;
       if (et < P.T) m->srow_ep[et] = p_row_scale(P, et);
+      // the active experts' tensor scales, read from shared memory by every
+      // expert unit of the launch (one L2 round trip here, none per unit)
+      for (int i = et; i < m->n_act; i += 128) {
+        const int e = m->act[i];
+        S.tsc(0)[e] = __ldg(P.ts_gate + e);
+        S.tsc(1)[e] = __ldg(P.ts_up + e);
+        S.tsc(2)[e] = __ldg(P.ts_down + e);
+      }
       epi_sync();
     } else if (ph == PH_DOWN && P.moe) {
       for (int i = et; i < kMaxT * 16; i += 128) (&m->comb_local[0][0])[i] = 0;
