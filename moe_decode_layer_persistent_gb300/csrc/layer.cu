@@ -34,6 +34,10 @@ namespace mk {
 // ------------------------------------------------------------ roles
 constexpr int kStagerBase = 160;   // warps 5-6
 constexpr int kEpiBase = 256;      // warps 8-11 (TMEM lane quadrants 0-3)
+// registers per thread: at launch (65536 / 384, rounded down to a multiple of
+// 8), for warp groups 0-1, for the epilogue warp group
+constexpr uint32_t kLaunchRegs = 168, kRegsRoles = 120, kRegsEpi = 256;
+static_assert(2 * 128 * kRegsRoles + 128 * kRegsEpi <= 384 * kLaunchRegs, "register split");
 
 // ------------------------------------------------------------ smem layout
 constexpr uint32_t kTileBytes = 16384;                       // 128 rows x 128 B
@@ -668,12 +672,6 @@ MK_DEV void prefetch_next_kv(const LayerParams& P) {
     }
 }
 
-// L2 prefetch of this CTA's 1/grid share of a bf16 weight matrix [N][K]
-// (128-row x 64-column tiles of its tensor map).
-MK_DEV void prefetch_share_l2(const LayerParams& P, const CUtensorMap* map, int N, int K) {
-  const int kt = K / 64, nt = (N + 127) / 128;
-  for (int i = blockIdx.x; i < nt * kt; i += P.grid) tma_prefetch_2d(map, (i % kt) * 64, (i / kt) * 128);
-}
 
 MK_DEV void run_producer(const LayerParams& P, const Smem& S) {
   Misc* m = S.m;
@@ -686,9 +684,9 @@ MK_DEV void run_producer(const LayerParams& P, const Smem& S) {
   for (int ph = 0; ph < PH_COUNT && ok; ++ph) {
     if (!phase_is_gemm(ph) || !phase_active(P, ph)) continue;
     if (P.moe && ph == PH_GU && !route_known) {
-      // HBM idles while the router picks the experts: fetch this CTA's share
-      // of the weights that do not depend on the routing (unpooler, fused
-      // next-layer QKV) into L2 meanwhile
+      // The unpooler and next-layer QKV weights are not fetched into L2 here:
+      // that 66 MB burst delayed the first gate/up tiles and the epilogues'
+      // stores more than it saved later (4.4 us per layer on the stack).
       if (P.pf_n > 0) {
         if (!prev_done) {
           pdl_wait();
@@ -696,8 +694,6 @@ MK_DEV void run_producer(const LayerParams& P, const Smem& S) {
         }
         prefetch_predicted_experts(P);
       }
-      prefetch_share_l2(P, &P.tm_unpool, P.H, P.P);
-      if (P.fuse_next) prefetch_share_l2(P, &P.tm_nqkv, P.Nqkv, P.H);
       if (!wait_bar(P, S, &m->route_ready, 0, ERR_TIMEOUT_ROUTE)) { ok = false; break; }
       route_known = true;
     }
@@ -2233,28 +2229,47 @@ __global__ void __launch_bounds__(kThreads, 1) mk_layer_kernel(const __grid_cons
   tc_fence_after();
   if (P.ts && threadIdx.x == 0) S.ts[PH_COUNT * kTsSlots] = t_start;
 
-  if (warp == 0) {
-    // weights depend on nothing in flight: stream them before the previous
-    // launch has finished
-    if (lane_id() == 0) run_producer(P, S);
-  } else {
+  // Register split: the producer, MMA, stager and image-builder warps (warp
+  // groups 0-1) need at most kRegsRoles registers; the epilogue warp group
+  // (GEMM epilogues, attention, merge, combine) gets the rest, so that it
+  // spills as little as possible (its local memory misses the 28 KB L1 that
+  // the shared-memory carve-out leaves).  Sum: 2*128*kRegsRoles +
+  // 128*kRegsEpi <= 384*168, the registers the block is launched with; both
+  // budgets go back to 168 before the common tail.  Each budget change sits
+  // inside its own branch, so that the compiler allocates each role's code
+  // for its own budget.
+  if (warp >= kEpiBase / 32) {
+    reg_alloc<kRegsEpi>();
     pdl_wait();
-    // One read of the launch epoch per CTA, before any of its arrivals: CTA 0
-    // advances the epoch only after every CTA has arrived on the last counter.
-    if (threadIdx.x == 32) m->epoch = *reinterpret_cast<volatile uint32_t*>(P.epoch);
-    named_bar(3, kThreads - 32);
-    if (threadIdx.x == 32) stamp(P, S, PH_COUNT, 1);
-    const uint32_t epoch = m->epoch;
-    if (warp >= 1 && warp <= 4) {
-      if (lane_id() == 0) run_mma(P, S);
-    } else if (warp == 5 || warp == 6) {
-      run_stager(P, S, epoch);
-    } else if (warp >= 8) {
-      run_epilogue(P, S, epoch);
-    } else if (warp == 7) {
-      if (blockIdx.x == 0 && P.pf_n > 0) prefetch_bookkeeping(P, S, epoch);
-      if (P.moe) build_expert_images(P, S, epoch);
+    named_bar(3, kThreads - 32);  // the launch epoch is read (below)
+    run_epilogue(P, S, m->epoch);
+    __syncwarp();
+    reg_dealloc<kLaunchRegs>();
+  } else {
+    reg_dealloc<kRegsRoles>();
+    if (warp == 0) {
+      // weights depend on nothing in flight: stream them before the previous
+      // launch has finished
+      if (lane_id() == 0) run_producer(P, S);
+    } else {
+      pdl_wait();
+      // One read of the launch epoch per CTA, before any of its arrivals: CTA 0
+      // advances the epoch only after every CTA has arrived on the last counter.
+      if (threadIdx.x == 32) m->epoch = *reinterpret_cast<volatile uint32_t*>(P.epoch);
+      named_bar(3, kThreads - 32);
+      if (threadIdx.x == 32) stamp(P, S, PH_COUNT, 1);
+      const uint32_t epoch = m->epoch;
+      if (warp >= 1 && warp <= 4) {
+        if (lane_id() == 0) run_mma(P, S);
+      } else if (warp == 5 || warp == 6) {
+        run_stager(P, S, epoch);
+      } else if (warp == 7) {
+        if (blockIdx.x == 0 && P.pf_n > 0) prefetch_bookkeeping(P, S, epoch);
+        if (P.moe) build_expert_images(P, S, epoch);
+      }
     }
+    __syncwarp();
+    reg_alloc<kLaunchRegs>();
   }
   tc_fence_before();
   __syncthreads();

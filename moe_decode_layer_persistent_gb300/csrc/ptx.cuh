@@ -286,6 +286,14 @@ MK_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "
 
 // ------------------------------------------------ programmatic dependent launch
 MK_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Per-warpgroup register budget (all four warps of a warpgroup execute the same
+// instruction, converged).  An increase waits until the CTA's decreases have
+// freed enough of the registers the block was launched with.
+template <uint32_t N>
+MK_DEV void reg_alloc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+template <uint32_t N>
+MK_DEV void reg_dealloc() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
 MK_DEV void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
