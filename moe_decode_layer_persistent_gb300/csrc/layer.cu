@@ -325,13 +325,18 @@ MK_DEV bool phase_active(const LayerParams& P, int ph) {
   }
 }
 
+// MoE down units: two adjacent 128-row tiles of one expert each (the last
+// unit of an odd tile count holds one), so that one copy of the expert's
+// image and one accumulator hand-off serve 256 output rows.
+MK_DEV int down_pairs(const LayerParams& P) { return (P.P / 128 + 1) / 2; }
+
 MK_DEV int phase_units(const LayerParams& P, const Smem& S, int ph) {
   switch (ph) {
     case PH_QKV: case PH_NQKV: return P.tiles_qkv * P.ks_qkv;
     case PH_O: return P.tiles_o * P.ks_o;
     case PH_RP: return P.moe ? (P.tiles_router + P.tiles_pool) * P.ks_rp : P.tiles_dgu * P.ks_dgu;
     case PH_GU: return S.m->n_act * (P.I / 128);
-    case PH_DOWN: return P.moe ? S.m->n_act * (P.P / 128) : P.tiles_ddown * P.ks_ddown;
+    case PH_DOWN: return P.moe ? S.m->n_act * down_pairs(P) : P.tiles_ddown * P.ks_ddown;
     case PH_UNPOOL: return P.tiles_unpool * P.ks_unpool;
     case PH_ATTN: return P.Hkv * P.attn_chunks;
     case PH_MERGE: return P.T * P.Hq;
@@ -380,9 +385,10 @@ MK_DEV int final_barrier(const LayerParams& P) { return P.fuse_next ? BAR_END : 
 struct Unit {
   const CUtensorMap* map[2];
   const uint8_t* sf[2];  // repacked scales of K-block 0 (NVFP4)
-  int pair;              // 1 or 2 weight matrices (gate + up)
+  int pair;              // 1 or 2 weight tiles (gate + up; two adjacent down tiles)
   int fp4;
   int row0;              // TMA row of the tile
+  int row1;              // TMA row of the second tile of a pair
   int x0;                // TMA x of K-block 0 (elements for bf16, bytes for NVFP4)
   int nkb;               // K-blocks of 128 bytes per row
   int tile;              // 128-row tile index within its matrix
@@ -415,7 +421,7 @@ MK_DEV Unit make_unit(const LayerParams& P, const Smem& S, int ph, int u) {
     }
     U.tile = U.col_tile - tile_base;
     U.ksplit = ks_count;
-    U.row0 = U.tile * 128;
+    U.row0 = U.row1 = U.tile * 128;
     const int kc = K / ks_count;
     U.x0 = U.ks * kc;
     U.nkb = kc / 64;
@@ -466,13 +472,14 @@ MK_DEV Unit make_unit(const LayerParams& P, const Smem& S, int ph, int u) {
       const bool gu = ph == PH_GU;
       const int N = gu ? P.I : P.P, K = gu ? P.P : P.I;
       const int tiles = N / 128;
-      const int e = S.m->act[u / tiles];
+      const int per = gu ? tiles : down_pairs(P);  // units per expert
+      const int e = S.m->act[u / per];
       U.fp4 = 1;
       U.expert = e;
-      U.tile = u % tiles;
+      U.tile = gu ? u % per : 2 * (u % per);
       U.ks = 0;
       U.ksplit = 1;
-      U.row0 = e * N + U.tile * 128;
+      U.row0 = U.row1 = e * N + U.tile * 128;
       U.x0 = 0;
       U.nkb = (K + 255) / 256;
       U.N = N;
@@ -487,6 +494,12 @@ MK_DEV Unit make_unit(const LayerParams& P, const Smem& S, int ph, int u) {
       } else {
         U.map[0] = &P.tm_down;
         U.sf[0] = P.sf_down + sf_off;
+        if (U.tile + 1 < tiles) {
+          U.pair = 2;
+          U.map[1] = &P.tm_down;
+          U.row1 = U.row0 + 128;
+          U.sf[1] = U.sf[0] + U.nkb * kSfBytes;
+        }
       }
       break;
     }
@@ -728,7 +741,7 @@ MK_DEV void run_producer(const LayerParams& P, const Smem& S) {
           if (P.ts) stamp_add(P, S, ph, 4, globaltimer() - w0);
           mbar_arrive_expect_tx(&m->full[stage], bytes);
           const int x = U.x0 + kb * (U.fp4 ? 128 : 64);
-          tma_load_2d(S.a_tile(stage), U.map[j], &m->full[stage], x, U.row0, pol);
+          tma_load_2d(S.a_tile(stage), U.map[j], &m->full[stage], x, j ? U.row1 : U.row0, pol);
           if (U.fp4) bulk_load(S.sf(stage), U.sf[j] + kb * kSfBytes, kSfBytes, &m->full[stage], pol);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
@@ -1604,12 +1617,20 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
       epi_sync();
       if (et == 0) red_release_add(P.exp_sync + e, 1u);
     } else {
+      // accumulator column i is the expert's i-th slot; the pair's second
+      // tile holds the next 128 features
       const float td = S.tsc(2)[e];
       for (int i = 0; i < n; ++i) {
         const int s = m->slots[m->off[e] + i];
-        P.z_buf[static_cast<size_t>(s) * P.P + f] = to_bf(g[i] * m->srow_ep[s] * td);
+        const float sr = m->srow_ep[s];
+        P.z_buf[static_cast<size_t>(s) * P.P + f] = to_bf(g[i] * sr * td);
+        if (U.pair == 2) P.z_buf[static_cast<size_t>(s) * P.P + f + 128] = to_bf(u[i] * sr * td);
       }
-      if (et < n) atomicAdd(&m->comb_local[m->slots[m->off[e] + et] / P.topk][U.tile], 1u);
+      if (et < n) {
+        const int t = m->slots[m->off[e] + et] / P.topk;
+        atomicAdd(&m->comb_local[t][U.tile], 1u);
+        if (U.pair == 2) atomicAdd(&m->comb_local[t][U.tile + 1], 1u);
+      }
     }
     return true;
   }

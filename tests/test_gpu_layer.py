@@ -45,6 +45,14 @@ def test_tiny_renormalised_topk(cuda_lib):
     _single(cuda_lib, "tiny_layer", "host", T=4, ctx=50, renorm=True, flips=True)
 
 
+def test_tiny_odd_down_tile_count(cuda_lib):
+    """pooled_dim 384: three 128-row down tiles per expert, so the down phase
+    has a unit of two tiles and a unit of one; and a gate/up K of 384 (one
+    full and one half NVFP4 K-block)."""
+    wl = dict(synth.WORKLOADS["tiny_layer"], pooled_dim=384, T=8, ctx=100)
+    _single(cuda_lib, wl, "host", flips=True)
+
+
 def test_swa_layer(cuda_lib):
     """16 verify tokens, context 8192, window 2048, 256 experts top-8."""
     _single(cuda_lib, "swa_layer", "cuda")
