@@ -243,9 +243,6 @@ MK_DEV void grp_count_in(const LayerParams& P, int kind, int g, uint32_t need, u
     st_release(grp_flag(P, kind, g), epoch + 1u);
   }
 }
-MK_DEV bool grp_ready(const LayerParams& P, int kind, int g, uint32_t epoch) {
-  return static_cast<int32_t>(ld_acquire(grp_flag(P, kind, g)) - (epoch + 1u)) >= 0;
-}
 // Does QKV tile t hold rows of group g (its 4 q heads, its k and v heads)?
 MK_DEV bool tile_in_group(const LayerParams& P, int t, int g) {
   const int a = t * 128, b = a + 128;
@@ -861,11 +858,24 @@ MK_DEV BfSrc bf_source(const LayerParams& P, int ph) {
   switch (ph) {
     case PH_QKV: return {P.x_in, P.H, P.attn_norm_w};
     case PH_NQKV: return {P.x_out, P.H, P.next_attn_norm_w};
-    case PH_O: return {P.o_buf, P.Hq * P.d, nullptr};
     case PH_RP: return {P.xmid, P.H, P.ffn_norm_w};
-    case PH_UNPOOL: return {P.y_buf, P.P, nullptr};
     default: return {P.a_buf, P.F, nullptr};  // dense down
   }
+}
+
+// bf16 operand images.  The o-proj input (the merged attention output) and
+// the unpooler input (the combined expert output) are written by their
+// producers straight into the layout of an operand buffer: K-blocks of 64
+// inputs, each 16 rows x 128 B (2048 B), SW128-swizzled.  A unit's token
+// operand is then one bulk copy of its K-slice (rows >= T hold whatever an
+// earlier step left: each row only reaches its own accumulator column, which
+// the epilogue does not read).
+MK_DEV uint32_t bf_image_off(int t, int k) {
+  return static_cast<uint32_t>(k >> 6) * 2048u + sw128_offset(t, (k & 63) * 2);
+}
+MK_DEV bool image_phase(int ph) { return ph == PH_O || ph == PH_UNPOOL; }
+MK_DEV const uint8_t* bf_image(const LayerParams& P, int ph) {
+  return reinterpret_cast<const uint8_t*>(ph == PH_O ? P.o_buf : P.y_buf);
 }
 
 MK_DEV void issue_bf16(const LayerParams& P, const Smem& S, int ph, const Unit& U, int buf) {
@@ -1128,6 +1138,55 @@ MK_DEV void issue_image(const LayerParams& P, const Smem& S, const uint8_t* img,
   bulk_load(S.bbuf(buf) + kBSfOff, img + half, half, lb, pol);
 }
 
+// The stagers through a phase whose token operand is a bf16 image (o-proj,
+// unpooler): per unit, once its buffer is free (and, for the o-proj, its
+// K-slice's head groups are merged), the leader bulk-copies the unit's
+// K-slice of the image into it.  With two buffers this runs one unit ahead of
+// the MMA.
+MK_DEV bool stage_image_phase(const LayerParams& P, const Smem& S, int ph, uint32_t epoch, QCursor& q,
+                              uint32_t (&b_ph)[2], uint32_t& ucount, uint32_t (&land_ph)[2]) {
+  Misc* m = S.m;
+  const int tid = threadIdx.x - kStagerBase;
+  const uint8_t* img = bf_image(P, ph);
+  int u;
+  if (!queue_pop_group(P, S, q, u, tid == 0, kBarStage, 64, 0)) return false;
+  while (u >= 0) {
+    const Unit U = make_unit(P, S, ph, u);
+    const uint32_t b = ucount & 1;
+    const uint64_t w0 = tnow(P);
+    if (!group_mbar_wait(P, S, &m->bempty[b], b_ph[b] ^ 1, ERR_TIMEOUT_B, tid == 0, kBarStage, 64, 0))
+      return false;
+    const uint64_t w1 = tnow(P);
+    if (ph == PH_O)
+      for (int g = o_group_lo(P, U); g <= o_group_hi(P, U); ++g)
+        if (!group_flag_wait(P, S, grp_flag(P, 2, g), epoch + 1u, tid == 0, kBarStage, 64, 0)) return false;
+    if (tid == 0) {
+      // the image was written by ordinary stores (of this and other CTAs),
+      // released to this thread: order them before its async-proxy copy
+      fence_proxy_async_global();
+      const uint32_t bytes = static_cast<uint32_t>(U.nkb) * 2048u;
+      uint64_t* lb = &m->land[b];
+      m->land_out[b] = 1;
+      mbar_arrive_expect_tx(lb, bytes);
+      bulk_load(S.bbuf(b), img + static_cast<size_t>(U.x0 / 64) * 2048, bytes, lb, policy_evict_normal());
+    }
+    if (!group_mbar_wait(P, S, &m->land[b], land_ph[b], ERR_TIMEOUT_B, tid == 0, kBarStage, 64, 0)) return false;
+    land_ph[b] ^= 1;
+    if (tid == 0) {
+      m->land_out[b] = 0;
+      mbar_arrive(&m->bfull[b]);
+      if (P.ts) {
+        stamp_add(P, S, ph, 8, w1 - w0);
+        stamp_add(P, S, ph, 9, globaltimer() - w1);
+      }
+    }
+    b_ph[b] ^= 1;
+    ++ucount;
+    if (!queue_pop_group(P, S, q, u, tid == 0, kBarStage, 64, 0)) return false;
+  }
+  return true;
+}
+
 // The stagers through one NVFP4 expert phase.  Each unit's operand is a copy
 // of an image, skipped when the buffer already holds that image (every gate/up
 // unit uses the p image; consecutive down units may share an expert).  A down
@@ -1282,28 +1341,24 @@ MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
       }
     }
     stage_sync();
-    // o-proj units wait for their own K-slice's head groups, not for the
-    // whole merge phase
-    const bool per_unit = ph == PH_O;
-    auto unit_ready = [&](const Unit& V) -> bool {  // non-blocking (leader)
-      for (int g = o_group_lo(P, V); g <= o_group_hi(P, V); ++g)
-        if (!grp_ready(P, 2, g, epoch)) return false;
-      return true;
-    };
     // The leader copies a unit's first inputs ahead into the buffer's landing
-    // area and records whether it did (read by all after the next barrier).
+    // area and records that it did (read by all after the next barrier).
     auto try_prefetch = [&](const Unit& V, int buf) {
       if (tid != 0) return;
-      const bool ready = !per_unit || unit_ready(V);
-      if (ready) issue_bf16(P, S, ph, V, buf);
-      m->pref_ok[buf] = ready ? 1 : 0;
+      issue_bf16(P, S, ph, V, buf);
+      m->pref_ok[buf] = 1;
     };
-    // attention keeps its tiles in the operand buffers: the o-proj (which no
-    // longer waits for every head group) starts once this CTA's attention is done
+    // attention keeps its tiles in the operand buffers: the o-proj (which
+    // waits per head group, not for the whole merge) starts once this CTA's
+    // attention is done
     if (ph == PH_O &&
         !group_mbar_wait(P, S, &m->attn_free, 0, ERR_TIMEOUT_B, tid == 0, kBarStage, 64, 0)) {
       ok = false;
       break;
+    }
+    if (image_phase(ph)) {
+      ok = stage_image_phase(P, S, ph, epoch, q, b_ph, ucount, land_ph);
+      continue;
     }
     // the phase's first unit, its inputs copied at once; later units' are
     // copied one unit ahead when the producer has already claimed them
@@ -1328,12 +1383,6 @@ MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
         break;
       }
       const bool pre = *reinterpret_cast<volatile int*>(&m->pref_ok[b]) != 0;
-      if (per_unit && !pre) {
-        // not ready when looked at ahead: wait for the unit's inputs now
-        for (int g = o_group_lo(P, U); g <= o_group_hi(P, U) && ok; ++g)
-          ok = group_flag_wait(P, S, grp_flag(P, 2, g), epoch + 1u, tid == 0, kBarStage, 64, 0);
-        if (!ok) break;
-      }
       const uint64_t w1 = tnow(P);
       const bool sok = stage_bf16(P, S, ph, U, b, pre, land_ph[b]);
       // both stager warps agree on the outcome before the next barrier
@@ -1988,9 +2037,13 @@ MK_DEV void merge_item(const LayerParams& P, int item) {
 #pragma unroll
     for (int v = 0; v < V; ++v) acc[v] += wgt * ov[v];
   }
-  __nv_bfloat16* out = P.o_buf + static_cast<size_t>(t) * P.Hq * D + hq * D + lane * V;
+  // this lane's V outputs lie in one 16-byte chunk of the o-proj input image
+  uint32_t w[V / 2];
 #pragma unroll
-  for (int v = 0; v < V; ++v) out[v] = to_bf(acc[v] / L);
+  for (int v = 0; v < V / 2; ++v) w[v] = pack_bf16(acc[2 * v] / L, acc[2 * v + 1] / L);
+  uint8_t* out = reinterpret_cast<uint8_t*>(P.o_buf) + bf_image_off(t, hq * D + lane * V);
+  if constexpr (V == 4) *reinterpret_cast<uint2*>(out) = make_uint2(w[0], w[1]);
+  else *reinterpret_cast<uint32_t*>(out) = w[0];
 }
 
 // End of the expert-down phase: publish this CTA's z contributions per
@@ -2054,7 +2107,7 @@ MK_DEV void combine_phase_end(const LayerParams& P, const Smem& S, int et) {
       const __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
       ow[j] = *reinterpret_cast<const uint32_t*>(&h);
     }
-    *reinterpret_cast<uint4*>(P.y_buf + static_cast<size_t>(t) * P.P + f0) = o;
+    *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(P.y_buf) + bf_image_off(t, f0)) = o;
   }
 }
 
