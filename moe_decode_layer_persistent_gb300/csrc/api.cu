@@ -376,6 +376,10 @@ mk_status mk_layer_create(const mk_layer_config* cfg, const mk_layer_weights* w,
   MK_TRY(dalloc(L, &P.xmid, T * P.H));
   MK_TRY(dalloc(L, &P.ssq_mid, T * (P.H / 128)));
   MK_TRY(dalloc(L, &P.ssq_out, T * (P.H / 128)));
+  if (P.fuse_next) {
+    MK_TRY(dalloc(L, &P.xn_img, T * P.H * 2));
+    MK_TRY(dalloc(L, &P.xt_flag, P.H / 128));
+  }
   size_t part = static_cast<size_t>(P.ks_qkv) * T * P.tiles_qkv * 128;
   part = std::max(part, static_cast<size_t>(P.ks_o) * T * P.tiles_o * 128);
   if (P.moe) {
@@ -417,6 +421,7 @@ mk_status mk_layer_create(const mk_layer_config* cfg, const mk_layer_weights* w,
   }
   MK_TRY(dalloc(L, &P.part, part));
   MK_TRY(dalloc(L, &P.part_o, static_cast<size_t>(P.ks_o) * T * P.tiles_o * 128));
+  if (P.fuse_next) MK_TRY(dalloc(L, &P.part_n, static_cast<size_t>(P.ks_qkv) * T * P.tiles_qkv * 128));
   L->attn_max_chunks = std::max(1, L->sm_count / P.Hkv);
   MK_TRY(dalloc(L, &P.attn_part,
                 static_cast<size_t>(P.Hkv) * L->attn_max_chunks * 64 * (P.d + 2)));
@@ -469,6 +474,7 @@ mk_status mk_layer_clear_status(mk_layer* layer) {
   if (P.comb_ctr)
     MK_CUDA_TRY(cudaMemset(P.comb_ctr, 0, kMaxT * (P.P / 128) * sizeof(uint32_t)));
   if (P.exp_sync) MK_CUDA_TRY(cudaMemset(P.exp_sync, 0, 2 * kMaxE * sizeof(uint32_t)));
+  if (P.xt_flag) MK_CUDA_TRY(cudaMemset(P.xt_flag, 0, (P.H / 128) * sizeof(uint32_t)));
   return MK_OK;
 }
 
@@ -800,6 +806,10 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_layer_config* cfg, const mk
   P.xmid = cv.take<__nv_bfloat16>(T * P.H);
   P.ssq_mid = cv.take<float>(T * (P.H / 128));
   P.ssq_out = cv.take<float>(T * (P.H / 128));
+  if (P.fuse_next) {
+    P.xn_img = cv.take<uint8_t>(T * P.H * 2);
+    P.xt_flag = cv.take<uint32_t>(P.H / 128);
+  }
   size_t part = static_cast<size_t>(P.ks_qkv) * T * P.tiles_qkv * 128;
   part = std::max(part, static_cast<size_t>(P.ks_o) * T * P.tiles_o * 128);
   size_t gu = 0, dn = 0;
@@ -833,6 +843,7 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_layer_config* cfg, const mk
   }
   P.part = cv.take<float>(part);
   P.part_o = cv.take<float>(static_cast<size_t>(P.ks_o) * T * P.tiles_o * 128);
+  if (P.fuse_next) P.part_n = cv.take<float>(static_cast<size_t>(P.ks_qkv) * T * P.tiles_qkv * 128);
   L.attn_max_chunks = std::min(kNoAllocMaxChunks, std::max(1, D.sm_count / P.Hkv));
   P.attn_part = cv.take<float>(static_cast<size_t>(P.Hkv) * L.attn_max_chunks * 64 * (P.d + 2));
   // counters that must start at zero each call: one contiguous block
@@ -863,6 +874,7 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_layer_config* cfg, const mk
   MK_CUDA_TRY(cudaMemsetAsync(zero, 0, (static_cast<size_t>(PH_COUNT) * 256 + 4 + kNumCounters + 2 + PH_COUNT +
                                         6 * kMaxGroups) * 4, s));
   if (P.comb_ctr) MK_CUDA_TRY(cudaMemsetAsync(P.comb_ctr, 0, T * (P.P / 128) * 4, s));
+  if (P.xt_flag) MK_CUDA_TRY(cudaMemsetAsync(P.xt_flag, 0, (P.H / 128) * 4, s));
   if (P.exp_sync) MK_CUDA_TRY(cudaMemsetAsync(P.exp_sync, 0, 2 * kMaxE * 4, s));
   if (P.moe) {
     // the operand images' padding past K must read as zero (an earlier call

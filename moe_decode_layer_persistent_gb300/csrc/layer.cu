@@ -83,6 +83,8 @@ struct Misc {
   float srow_st[kMaxT];            // stager: row scales of p (its share of the p image)
   float srow_b[kMaxT];             // warp 7: row scales of the expert image it builds
   float srow_ep[kMaxT * kMaxK];    // epilogue: NVFP4 row scales of the phase input
+  float rnorm_ep[kMaxT];           // epilogue: RMS factors of x_out (fused next-layer QKV)
+  int rn_ready;                    // epilogue: rnorm_ep computed in this launch
   float red[4][kMaxT];             // epilogue cross-warp reductions
   uint32_t comb_local[kMaxT][16];  // epilogue: this CTA's z contributions per (token, tile)
   int done_pairs[kMaxT * 16];      // epilogue: (token, tile) pairs this CTA completes
@@ -358,7 +360,7 @@ MK_DEV int phase_dep(const LayerParams& P, int ph) {
     case PH_GU: return -1;                     // the p image (misc_ctr[2])
     case PH_DOWN: return P.moe ? -1 : BAR_RP;  // MoE: per expert (exp_sync)
     case PH_UNPOOL: return BAR_DOWN;
-    case PH_NQKV: return BAR_X;
+    case PH_NQKV: return -1;  // per 128-column tile of x_out (xt_flag)
   }
   return -1;
 }
@@ -409,12 +411,14 @@ MK_DEV Unit make_unit(const LayerParams& P, const Smem& S, int ph, int u) {
     U.fp4 = 0;
     U.col_tile = u / ks_count;
     U.ks = u % ks_count;
-    if (ph == PH_QKV || ph == PH_NQKV) {
+    if (ph == PH_QKV) {
       U.col_tile = u / ks_count < 64 ? P.qkv_order[u / ks_count] : u / ks_count;  // group by group
-    } else if (ph == PH_O) {
-      // K-slice by K-slice: each slice is one group's merged heads
-      U.col_tile = u % P.tiles_o;
-      U.ks = u / P.tiles_o;
+    } else if (ph == PH_O || ph == PH_NQKV) {
+      // K-slice by K-slice: an o-proj slice is one group's merged heads; a
+      // next-layer QKV slice waits for the tiles of x_out it covers
+      const int nt = ph == PH_O ? P.tiles_o : P.tiles_qkv;
+      U.col_tile = u % nt;
+      U.ks = u / nt;
     }
     U.tile = U.col_tile - tile_base;
     U.ksplit = ks_count;
@@ -873,8 +877,9 @@ MK_DEV BfSrc bf_source(const LayerParams& P, int ph) {
 MK_DEV uint32_t bf_image_off(int t, int k) {
   return static_cast<uint32_t>(k >> 6) * 2048u + sw128_offset(t, (k & 63) * 2);
 }
-MK_DEV bool image_phase(int ph) { return ph == PH_O || ph == PH_UNPOOL; }
+MK_DEV bool image_phase(int ph) { return ph == PH_O || ph == PH_UNPOOL || ph == PH_NQKV; }
 MK_DEV const uint8_t* bf_image(const LayerParams& P, int ph) {
+  if (ph == PH_NQKV) return P.xn_img;
   return reinterpret_cast<const uint8_t*>(ph == PH_O ? P.o_buf : P.y_buf);
 }
 
@@ -888,6 +893,9 @@ MK_DEV void issue_bf16(const LayerParams& P, const Smem& S, int ph, const Unit& 
   const uint64_t pol = policy_evict_normal();
   uint64_t* lb = &S.m->land[buf];
   S.m->land_out[buf] = 1;
+  // the rows were written by ordinary stores (of this and other CTAs),
+  // released to this thread: order them before its async-proxy copies
+  fence_proxy_async_global();
   mbar_arrive_expect_tx(lb, P.T * rowbytes + (src.gain ? rowbytes : 0u));
   for (int t = 0; t < P.T; ++t)
     bulk_load(raw + t * rowbytes, src.src + static_cast<size_t>(t) * src.ld + U.x0, rowbytes, lb, pol);
@@ -1139,9 +1147,10 @@ MK_DEV void issue_image(const LayerParams& P, const Smem& S, const uint8_t* img,
 }
 
 // The stagers through a phase whose token operand is a bf16 image (o-proj,
-// unpooler): per unit, once its buffer is free (and, for the o-proj, its
-// K-slice's head groups are merged), the leader bulk-copies the unit's
-// K-slice of the image into it.  With two buffers this runs one unit ahead of
+// unpooler, fused next-layer QKV): per unit, once its buffer is free and its
+// K-slice is written (o-proj: its head groups merged; next-layer QKV: the
+// tiles of x_out it covers), the leader bulk-copies the unit's K-slice of the
+// image into it.  With two buffers this runs one unit ahead of
 // the MMA.
 MK_DEV bool stage_image_phase(const LayerParams& P, const Smem& S, int ph, uint32_t epoch, QCursor& q,
                               uint32_t (&b_ph)[2], uint32_t& ucount, uint32_t (&land_ph)[2]) {
@@ -1160,6 +1169,9 @@ MK_DEV bool stage_image_phase(const LayerParams& P, const Smem& S, int ph, uint3
     if (ph == PH_O)
       for (int g = o_group_lo(P, U); g <= o_group_hi(P, U); ++g)
         if (!group_flag_wait(P, S, grp_flag(P, 2, g), epoch + 1u, tid == 0, kBarStage, 64, 0)) return false;
+    if (ph == PH_NQKV)
+      for (int j = U.x0 / 128; j <= (U.x0 + U.nkb * 64 - 1) / 128; ++j)
+        if (!group_flag_wait(P, S, P.xt_flag + j, epoch + 1u, tid == 0, kBarStage, 64, 0)) return false;
     if (tid == 0) {
       // the image was written by ordinary stores (of this and other CTAs),
       // released to this thread: order them before its async-proxy copy
@@ -1333,10 +1345,9 @@ MK_DEV void run_stager(const LayerParams& P, const Smem& S, uint32_t epoch) {
     }
     if (tid == 0) stamp(P, S, ph, 14);
     // per-phase inputs of the token operand
-    if (ph == PH_RP || ph == PH_NQKV) {
-      const float* ssq = ph == PH_RP ? P.ssq_mid : P.ssq_out;
+    if (ph == PH_RP) {
       if (tid < P.T) {
-        const float s = reduce_partials<false>(ssq + tid, P.H / 128, kMaxT);
+        const float s = reduce_partials<false>(P.ssq_mid + tid, P.H / 128, kMaxT);
         m->rnorm[tid] = 1.0f / sqrtf(s / P.H + P.eps);
       }
     }
@@ -1492,6 +1503,8 @@ MK_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : 
 // The residual phases (o-proj, unpooler, dense down) add the layer input
 // x_in (o-proj) or x_mid to their output.
 MK_DEV bool residual_phase(int ph) { return ph == PH_O || ph == PH_UNPOOL || ph == PH_DOWN; }
+// The phase whose final step writes x_out.
+MK_DEV int x_out_phase(const LayerParams& P) { return P.moe ? PH_UNPOOL : PH_DOWN; }
 MK_DEV const __nv_bfloat16* residual_src(const LayerParams& P, int ph) { return ph == PH_O ? P.x_in : P.xmid; }
 // Asynchronous copy of a tile's residual rows (T rows of 128 columns from
 // U.row0) into the epilogue's staging area: two 16-byte chunks per thread,
@@ -1524,7 +1537,7 @@ MK_DEV void epi_bf16_final(const LayerParams& P, const Smem& S, int ph, const Un
       __nv_bfloat16* vc = ph == PH_QKV ? P.v_cache : P.nv_cache;
       const int nq = P.Hq * P.d, nk = P.Hkv * P.d;
       for (int t = 0; t < P.T; ++t) {
-        const __nv_bfloat16 v = to_bf(g[t]);
+        const __nv_bfloat16 v = to_bf(ph == PH_NQKV ? g[t] * S.m->rnorm_ep[t] : g[t]);
         if (f < nq) qdst[static_cast<size_t>(t) * nq + f] = v;
         else if (f < nq + nk) kc[static_cast<size_t>(P.ctx + t) * nk + (f - nq)] = v;
         else vc[static_cast<size_t>(P.ctx + t) * nk + (f - nq - nk)] = v;
@@ -1535,6 +1548,10 @@ MK_DEV void epi_bf16_final(const LayerParams& P, const Smem& S, int ph, const Un
     case PH_UNPOOL:
     case PH_DOWN: {  // residual: x = bf16(res + acc); sum-of-squares partial
       __nv_bfloat16* dst = ph == PH_O ? P.xmid : P.x_out;
+      // the phase that writes x_out also writes the fused next-layer QKV's
+      // operand image, bf16(x_out * gain)
+      const bool xn = P.fuse_next && ph == x_out_phase(P);
+      const float gn = xn && valid ? __bfloat162float(P.next_attn_norm_w[f]) : 0.f;
       // every residual load is issued before the first store: a load may not
       // move past a store that could alias it, so interleaving them would cost
       // one memory round trip per token
@@ -1558,6 +1575,7 @@ MK_DEV void epi_bf16_final(const LayerParams& P, const Smem& S, int ph, const Un
         if (valid && t < P.T) {
           const float x = round_bf(rv[t] + g[t]);
           dst[static_cast<size_t>(t) * P.H + f] = to_bf(x);
+          if (xn) *reinterpret_cast<__nv_bfloat16*>(P.xn_img + bf_image_off(t, f)) = to_bf(x * gn);
           sq[t] = x * x;
         }
       }
@@ -1687,8 +1705,9 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
   // bf16 phase: split-K partials + fix-up by the last arriving unit of a tile
   bool staged = false;
   if (U.ksplit > 1) {
-    // the o-proj overlaps the QKV phase (per head group), so it has its own
-    float* part = ph == PH_O ? P.part_o : P.part;
+    // the o-proj overlaps the QKV phase (per head group) and the fused
+    // next-layer QKV the fix-ups of the phase before it, so each has its own
+    float* part = ph == PH_O ? P.part_o : ph == PH_NQKV ? P.part_n : P.part;
     // partials: part[ks][j][col][16 tokens], col = col_tile * 128 + row in
     // tile: each thread moves its 16 token values as four 16-byte vectors
     const size_t ncol = static_cast<size_t>(U.col_tiles) * 128;
@@ -1719,10 +1738,13 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
       float acc[kMaxT];
 #pragma unroll
       for (int t = 0; t < kMaxT; ++t) acc[t] = 0.f;
-      for (int ks = 0; ks < U.ksplit; ks += 4) {
-        float4 v[4][4];
+      // the partials are summed in split order, kFixBatch splits' loads at a
+      // time (more would not fit in registers)
+      constexpr int kFixBatch = 4;
+      for (int ks = 0; ks < U.ksplit; ks += kFixBatch) {
+        float4 v[kFixBatch][4];
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
+        for (int kk = 0; kk < kFixBatch; ++kk) {
           if (ks + kk < U.ksplit) {
             const float4* src = reinterpret_cast<const float4*>(
                 part + ((static_cast<size_t>((ks + kk) * U.pair + j)) * ncol + col) * kMaxT);
@@ -1731,7 +1753,7 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
           }
         }
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
+        for (int kk = 0; kk < kFixBatch; ++kk) {
           if (ks + kk < U.ksplit) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -1747,7 +1769,23 @@ MK_DEV bool epi_gemm_unit(const LayerParams& P, const Smem& S, int ph, const Uni
       for (int t = 0; t < kMaxT; ++t) (j ? u : g)[t] = acc[t];
     }
   }
+  if (ph == PH_NQKV && !m->rn_ready) {
+    // The next-layer QKV ran on bf16(x_out * gain): its RMS factors, once
+    // per launch, when every tile of x_out (and its sum-of-squares partial)
+    // is in.
+    if (!group_grid_wait(P, S, BAR_X, grid_target(P, m->epoch), et == 0, kBarEpi, 128, 1)) return false;
+    if (et < P.T)
+      m->rnorm_ep[et] = 1.0f / sqrtf(reduce_partials<false>(P.ssq_out + et, P.H / 128, kMaxT) / P.H + P.eps);
+    if (et == 0) m->rn_ready = 1;
+    epi_sync();
+  }
   epi_bf16_final(P, S, ph, U, et, g, u, staged);
+  if (P.fuse_next && ph == x_out_phase(P)) {
+    // this tile of x_out, its image columns and its sum-of-squares partial
+    // are final: the next-layer QKV units of its K-slices may start
+    epi_sync();
+    if (et == 0) st_release(P.xt_flag + U.tile, m->epoch + 1u);
+  }
   if (ph == PH_QKV) {
     // this tile's q, k and v rows are final: count it in for its groups (a
     // counter that grows by grp_tiles per launch; no reply is waited for)
@@ -2291,6 +2329,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_layer_kernel(const __grid_cons
     for (int i = 0; i < 2; ++i) mbar_init(&m->land[i], 1);
     m->abort = 0;
     m->n_act = 0;
+    m->rn_ready = 0;
     for (int i = 0; i < 2; ++i) m->land_out[i] = 0;
     fence_mbar_init();
   }

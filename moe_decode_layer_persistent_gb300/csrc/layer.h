@@ -131,11 +131,19 @@ struct LayerParams {
   // MoE: the expert MMAs' token operands, NVFP4-quantised once per launch in
   // the layout of a shared-memory operand buffer (image_bytes(K) each: codes
   // in K-blocks of 2048 B -- 16 rows x 128 B, 128-byte swizzle -- then the
-  // 512-byte scale chunks).  pq_img: p of all T tokens (row t = token t), a
-  // 1/grid share by every CTA once p is complete; aq_img [E]: the SwiGLU rows
-  // of expert e in slot order, by the CTA that finishes e's last gate/up tile.
+  // 512-byte scale chunks).  pq_img: p of all T tokens (row t = token t),
+  // quantised in shares by the CTAs without a top-k token once p is complete;
+  // aq_img [E]: the SwiGLU rows of expert e in slot order, by warp 7 of CTA
+  // (e's active index) mod grid once all of e's gate/up tiles are in.
   uint8_t* pq_img;
   uint8_t* aq_img;
+  // Fused next-layer QKV: its token operand bf16(x_out * gain) (the RMS
+  // factor is applied after the projection) as a bf16 operand image (H/64
+  // K-blocks of 2048 B: 16 rows x 128 B, 128-byte swizzle), written by the
+  // final step of each 128-column tile of x_out; xt_flag [H/128]: that tile's
+  // image columns and sum-of-squares partial written (epoch + 1).
+  uint8_t* xn_img;
+  uint32_t* xt_flag;
   uint32_t* misc_ctr;       // [0]: router tiles done, [1]: pooler tiles done,
                             // [2]: p and its amax partials complete (epoch + 1),
                             // [3]: router logits complete (epoch + 1)
@@ -165,6 +173,8 @@ struct LayerParams {
   uint8_t qkv_order[64];           // QKV tile taken in claim position i (< 64): group by group
   uint8_t grp_tiles[kMaxGroups];   // QKV tiles holding rows of group g
   float* part_o;            // split-K partials of the o-proj (it overlaps the QKV phase)
+  float* part_n;            // split-K partials of the fused next-layer QKV (it overlaps
+                            // the fix-ups of the phase that writes x_out)
 };
 constexpr int kTsSlots = 16;
 
