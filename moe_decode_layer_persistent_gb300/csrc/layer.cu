@@ -2046,10 +2046,15 @@ MK_DEV void attention_unit(const LayerParams& P, const Smem& S, int g, int lo, i
 }
 
 // Merge of the attention partials of one (token, q head) by one warp:
-// o = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c over the chunks c.
+// o = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c over the chunks c, summed
+// in chunk order.  The loads go out in batches (the chunk statistics one chunk
+// per lane, the o partials 16 chunks at a time, the first batch together with
+// the statistics), so that a merge costs a few L2 round trips, not one per
+// four chunks.
 template <int D>
 MK_DEV void merge_item(const LayerParams& P, int item) {
   constexpr int V = D / 32;  // output elements per lane
+  constexpr int kB = 16;     // chunks whose o partials are loaded together (divides 32)
   const int lane = lane_id();
   const int t = item / P.Hq, hq = item % P.Hq;
   const int g = hq / 4, hl = hq % 4;
@@ -2057,23 +2062,52 @@ MK_DEV void merge_item(const LayerParams& P, int item) {
   const size_t stride = static_cast<size_t>(64) * (D + 2);
   const float* base = P.attn_part + static_cast<size_t>(g * P.attn_chunks) * stride +
                       static_cast<size_t>(row) * (D + 2);
-  float M = -INFINITY;
-  for (int c = lane; c < P.attn_chunks; c += 32) M = fmaxf(M, __ldcg(base + c * stride + D));
+  const int C = P.attn_chunks;
+  // chunk statistics of the first 32 chunks (lane j: chunk j) and the first
+  // batch of o partials go out together; then the maximum over all chunks
+  float mc = -INFINITY, lc = 0.f;
+  if (lane < C) {
+    mc = __ldcg(base + lane * stride + D);
+    lc = __ldcg(base + lane * stride + D + 1);
+  }
+  float ov[kB][V];
+#pragma unroll
+  for (int j = 0; j < kB; ++j)
+#pragma unroll
+    for (int v = 0; v < V; ++v) ov[j][v] = j < C ? __ldcg(base + j * stride + lane * V + v) : 0.f;
+  float M = mc;
+  for (int c = lane + 32; c < C; c += 32) M = fmaxf(M, __ldcg(base + c * stride + D));
   M = warp_max(M);
+  float wl = mc == -INFINITY ? 0.f : exp2f(mc - M);
   float acc[V], L = 0.f;
 #pragma unroll
   for (int v = 0; v < V; ++v) acc[v] = 0.f;
-#pragma unroll 4
-  for (int c = 0; c < P.attn_chunks; ++c) {
-    const float* pc = base + c * stride;
-    const float mc = __ldcg(pc + D), lc = __ldcg(pc + D + 1);
-    float ov[V];
+  for (int c0 = 0; c0 < C; c0 += kB) {
+    if (c0 > 0) {
+      if ((c0 & 31) == 0) {  // the next group of 32 chunks' statistics
+        mc = -INFINITY;
+        lc = 0.f;
+        if (c0 + lane < C) {
+          mc = __ldcg(base + (c0 + lane) * stride + D);
+          lc = __ldcg(base + (c0 + lane) * stride + D + 1);
+        }
+        wl = mc == -INFINITY ? 0.f : exp2f(mc - M);
+      }
 #pragma unroll
-    for (int v = 0; v < V; ++v) ov[v] = __ldcg(pc + lane * V + v);
-    const float wgt = mc == -INFINITY ? 0.f : exp2f(mc - M);
-    L += wgt * lc;
+      for (int j = 0; j < kB; ++j)
 #pragma unroll
-    for (int v = 0; v < V; ++v) acc[v] += wgt * ov[v];
+        for (int v = 0; v < V; ++v)
+          ov[j][v] = c0 + j < C ? __ldcg(base + (c0 + j) * stride + lane * V + v) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < kB; ++j) {
+      if (c0 + j < C) {  // the same for every lane
+        const float wgt = __shfl_sync(0xffffffffu, wl, (c0 + j) & 31);
+        L += wgt * __shfl_sync(0xffffffffu, lc, (c0 + j) & 31);
+#pragma unroll
+        for (int v = 0; v < V; ++v) acc[v] += wgt * ov[j][v];
+      }
+    }
   }
   // this lane's V outputs lie in one 16-byte chunk of the o-proj input image
   uint32_t w[V / 2];
