@@ -428,7 +428,7 @@ mk_status mk_layer_create(const mk_layer_config* cfg, const mk_layer_weights* w,
   MK_TRY(dalloc(L, &P.fix_ctr, static_cast<size_t>(PH_COUNT) * 256));
   MK_TRY(dalloc(L, &P.misc_ctr, 4));
   MK_TRY(dalloc(L, &P.sched, PH_COUNT));
-  MK_TRY(dalloc(L, &P.grp_sync, 6 * kMaxGroups));
+  MK_TRY(dalloc(L, &P.grp_sync, 3 * kMaxGroups));
   MK_TRY(dalloc(L, &P.bar_ctr, kNumCounters));
   MK_TRY(dalloc(L, &P.epoch, 1));
   MK_TRY(dalloc(L, &P.status, 1));
@@ -470,7 +470,7 @@ mk_status mk_layer_clear_status(mk_layer* layer) {
   MK_CUDA_TRY(cudaMemset(P.fix_ctr, 0, PH_COUNT * 256 * sizeof(uint32_t)));
   MK_CUDA_TRY(cudaMemset(P.misc_ctr, 0, 4 * sizeof(uint32_t)));
   MK_CUDA_TRY(cudaMemset(P.sched, 0, PH_COUNT * sizeof(uint32_t)));
-  MK_CUDA_TRY(cudaMemset(P.grp_sync, 0, 6 * kMaxGroups * sizeof(uint32_t)));
+  MK_CUDA_TRY(cudaMemset(P.grp_sync, 0, 3 * kMaxGroups * sizeof(uint32_t)));
   if (P.comb_ctr)
     MK_CUDA_TRY(cudaMemset(P.comb_ctr, 0, kMaxT * (P.P / 128) * sizeof(uint32_t)));
   if (P.exp_sync) MK_CUDA_TRY(cudaMemset(P.exp_sync, 0, 2 * kMaxE * sizeof(uint32_t)));
@@ -848,7 +848,7 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_layer_config* cfg, const mk
   P.attn_part = cv.take<float>(static_cast<size_t>(P.Hkv) * L.attn_max_chunks * 64 * (P.d + 2));
   // counters that must start at zero each call: one contiguous block
   uint32_t* zero = cv.take<uint32_t>(static_cast<size_t>(PH_COUNT) * 256 + 4 + kNumCounters + 2 + PH_COUNT +
-                                     6 * kMaxGroups);
+                                     3 * kMaxGroups);
   if (cv.overflow) {
     if (log_enabled())
       std::fprintf(stderr, "mk: mk_decode_step_noalloc: this layer needs more than the %zu-byte scratch\n",
@@ -872,7 +872,7 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_layer_config* cfg, const mk
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   MK_CUDA_TRY(cudaMemsetAsync(zero, 0, (static_cast<size_t>(PH_COUNT) * 256 + 4 + kNumCounters + 2 + PH_COUNT +
-                                        6 * kMaxGroups) * 4, s));
+                                        3 * kMaxGroups) * 4, s));
   if (P.comb_ctr) MK_CUDA_TRY(cudaMemsetAsync(P.comb_ctr, 0, T * (P.P / 128) * 4, s));
   if (P.xt_flag) MK_CUDA_TRY(cudaMemsetAsync(P.xt_flag, 0, (P.H / 128) * 4, s));
   if (P.exp_sync) MK_CUDA_TRY(cudaMemsetAsync(P.exp_sync, 0, 2 * kMaxE * 4, s));

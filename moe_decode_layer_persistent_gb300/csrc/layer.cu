@@ -229,22 +229,13 @@ MK_DEV bool group_flag_wait(const LayerParams& P, const Smem& S, const uint32_t*
 
 // ------------------------------------------------------------ per-group dataflow
 // QKV -> attention -> merge -> o-proj proceed per KV-head group g: kind 0
-// counts g's finished QKV tiles, 1 its attention chunks, 2 its merged
-// (token, head) items; the last arrival resets the counter and releases the
-// kind's ready flag with the launch's epoch + 1.
+// counts g's finished QKV tiles (it grows by the group's tile count per launch),
+// 1 its attention chunks, 2 its merged (token, head) items (both reset by CTA 0
+// at the end of a launch: their counts per launch change with ctx and T).  A
+// thread counts in with a release once the data it counts is written (by it,
+// or by its group before a barrier) and waits for no reply; a waiter acquires
+// the counter against the launch's target.
 MK_DEV uint32_t* grp_ctr(const LayerParams& P, int kind, int g) { return P.grp_sync + kind * kMaxGroups + g; }
-MK_DEV uint32_t* grp_flag(const LayerParams& P, int kind, int g) {
-  return P.grp_sync + (3 + kind) * kMaxGroups + g;
-}
-// One thread, after the data it counts is written (by it, or by its group
-// before a barrier): the arrival releases it.
-MK_DEV void grp_count_in(const LayerParams& P, int kind, int g, uint32_t need, uint32_t epoch) {
-  uint32_t* c = grp_ctr(P, kind, g);
-  if (atom_add_acq_rel(c, 1u) == need - 1u) {
-    *c = 0;
-    st_release(grp_flag(P, kind, g), epoch + 1u);
-  }
-}
 // Does QKV tile t hold rows of group g (its 4 q heads, its k and v heads)?
 MK_DEV bool tile_in_group(const LayerParams& P, int t, int g) {
   const int a = t * 128, b = a + 128;
@@ -1168,7 +1159,8 @@ MK_DEV bool stage_image_phase(const LayerParams& P, const Smem& S, int ph, uint3
     const uint64_t w1 = tnow(P);
     if (ph == PH_O)
       for (int g = o_group_lo(P, U); g <= o_group_hi(P, U); ++g)
-        if (!group_flag_wait(P, S, grp_flag(P, 2, g), epoch + 1u, tid == 0, kBarStage, 64, 0)) return false;
+        if (!group_flag_wait(P, S, grp_ctr(P, 2, g), static_cast<uint32_t>(P.T * 4), tid == 0, kBarStage, 64, 0))
+          return false;
     if (ph == PH_NQKV)
       for (int j = U.x0 / 128; j <= (U.x0 + U.nkb * 64 - 1) / 128; ++j)
         if (!group_flag_wait(P, S, P.xt_flag + j, epoch + 1u, tid == 0, kBarStage, 64, 0)) return false;
@@ -2225,7 +2217,7 @@ MK_DEV void run_epilogue(const LayerParams& P, const Smem& S, uint32_t epoch) {
           else attention_unit<64, false>(P, S, g, lo, hi, c, et);
         }
         epi_sync();
-        if (et == 0) grp_count_in(P, 1, g, P.attn_chunks, epoch);
+        if (et == 0) red_release_add(grp_ctr(P, 1, g), 1u);  // no reply waited for
       }
       if (!ok) break;
       if (et == 0) {
@@ -2245,13 +2237,14 @@ MK_DEV void run_epilogue(const LayerParams& P, const Smem& S, uint32_t epoch) {
         if ((k & 3) != w) continue;  // the CTA's k-th item goes to warp k % 4
         const int g = (u % P.Hq) / 4;
         int r = 1;
-        if (lane_id() == 0) r = flag_wait(P, S, grp_flag(P, 1, g), epoch + 1u, ERR_TIMEOUT_DATA) ? 1 : 0;
+        if (lane_id() == 0)
+          r = flag_wait(P, S, grp_ctr(P, 1, g), static_cast<uint32_t>(P.attn_chunks), ERR_TIMEOUT_DATA) ? 1 : 0;
         if (!(wok = __shfl_sync(0xffffffffu, r, 0) != 0)) break;
         __syncwarp();  // the lanes' loads below follow lane 0's acquire
         if (P.d == 128) merge_item<128>(P, u);
         else merge_item<64>(P, u);
         __syncwarp();
-        if (lane_id() == 0) grp_count_in(P, 2, g, static_cast<uint32_t>(P.T * 4), epoch);
+        if (lane_id() == 0) red_release_add(grp_ctr(P, 2, g), 1u);  // no reply waited for
       }
       // the epilogue warps agree on the outcome before their next barrier
       if (lane_id() == 0) m->red[0][w] = wok ? 1.f : 0.f;
@@ -2317,6 +2310,8 @@ MK_DEV void run_epilogue(const LayerParams& P, const Smem& S, uint32_t epoch) {
       // tile: the claim and per-expert counters start the next launch at zero
       if (P.moe)
         for (int i = et; i < P.E; i += 128) P.exp_sync[i] = 0;
+      // and the per-group attention-chunk and merge-item counters
+      for (int i = et; i < 2 * kMaxGroups; i += 128) grp_ctr(P, 1, 0)[i] = 0;
       epi_sync();
       if (et == 0) {
         for (int i = 0; i < PH_COUNT; ++i) P.sched[i] = 0;

@@ -167,8 +167,9 @@ struct LayerParams {
   // start, inputs ready, kernel end, router top-k start and release.
   uint64_t* ts;
   // per KV-head group dataflow QKV -> attention -> merge -> o-proj:
-  // [0..2][kMaxGroups] counters (finished QKV tiles, attention chunks, merge
-  // items; the last arrival resets it), [3..5][kMaxGroups] ready flags (epoch + 1)
+  // [0..2][kMaxGroups] counters: finished QKV tiles (growing by the group's
+  // tile count per launch), attention chunks and merge items (reset by CTA 0
+  // at the end of a launch)
   uint32_t* grp_sync;
   uint8_t qkv_order[64];           // QKV tile taken in claim position i (< 64): group by group
   uint8_t grp_tiles[kMaxGroups];   // QKV tiles holding rows of group g
