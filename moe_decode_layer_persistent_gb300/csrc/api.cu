@@ -41,12 +41,15 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Split of a bf16 contraction over K into units of at most 8 K-blocks (512
-// inputs) that divide K evenly.
-int choose_ksplit(int K) {
+// Split of a bf16 contraction over K into units of at most max_kb K-blocks
+// (64 inputs each) that divide K evenly.  Units whose token operand is staged
+// through the landing area hold at most 8 K-blocks; units that copy an operand
+// image straight into the 40 KB operand buffer hold up to 16.
+constexpr int kImageMaxKb = 16;
+int choose_ksplit(int K, int max_kb = 8) {
   const int nkb = K / 64;
   for (int ks = 1; ks <= nkb; ++ks)
-    if (nkb % ks == 0 && nkb / ks <= 8) return ks;
+    if (nkb % ks == 0 && nkb / ks <= max_kb) return ks;
   return nkb;
 }
 
@@ -327,7 +330,7 @@ mk_status mk_layer_create(const mk_layer_config* cfg, const mk_layer_weights* w,
   P.ks_qkv = choose_ksplit(P.H);
   P.tiles_qkv = (P.Nqkv + 127) / 128;
   qkv_group_order(P);
-  P.ks_o = choose_ksplit(P.Hq * P.d);
+  P.ks_o = choose_ksplit(P.Hq * P.d, kImageMaxKb);
   P.tiles_o = P.H / 128;
   P.ks_rp = choose_ksplit(P.H);
   if (P.moe) {
@@ -754,7 +757,7 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_layer_config* cfg, const mk
   P.ks_qkv = choose_ksplit(P.H);
   P.tiles_qkv = (P.Nqkv + 127) / 128;
   qkv_group_order(P);
-  P.ks_o = choose_ksplit(P.Hq * P.d);
+  P.ks_o = choose_ksplit(P.Hq * P.d, kImageMaxKb);
   P.tiles_o = P.H / 128;
   P.ks_rp = choose_ksplit(P.H);
   if (P.moe) {
