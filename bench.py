@@ -143,8 +143,8 @@ def kernel_source_hash(files=None):
 def profiled(workload):
     """Figures per launch from the committed ncu summary of this workload
     (profiles/mk_layer_kernel_<workload>.md): DRAM bytes read + written
-    (traffic_bytes_per_launch) and the tensor pipe's share of the expert
-    phases (tensor_pipe), or {} when there is none or the kernel sources
+    (traffic_bytes_per_launch) and the tensor pipe's share of the launch's
+    cycles (tensor_pipe), or {} when there is none or the kernel sources
     changed since it was captured."""
     path = os.path.join(ROOT, "profiles", "mk_layer_kernel_%s.md" % workload)
     if not os.path.exists(path):
@@ -537,7 +537,7 @@ def main():
                      "algorithmic_bytes_per_launch": int(alg_per_launch),
                      "launch_us_mean": round(launch_s * 1e6, 3),
                      "traffic": prof.get("traffic_bytes_per_launch"),
-                     "tensor_pipe_expert_phases": prof.get("tensor_pipe")},
+                     "tensor_pipe": prof.get("tensor_pipe")},
         "e2e": {"value": round(e2e_ms * 1e3, 3), "unit": "us/step",
                 "h2d_bytes_per_step": bytes_io, "d2h_bytes_per_step": bytes_io},
         "gpu_launches": args.steps * R.launches_per_step,
