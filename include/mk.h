@@ -64,7 +64,12 @@ typedef enum {
 
 /* mk_layer_config.flags */
 #define MK_FIRST_LAYER   0x1u  /* run RMSNorm + QKV + KV write on x_in first     */
-#define MK_FUSE_NEXT_QKV 0x2u  /* end with the next layer's RMSNorm+QKV+KV write */
+#define MK_FUSE_NEXT_QKV 0x2u  /* end with the next layer's RMSNorm+QKV+KV write;
+                                  it projects bf16(x_out * gain) and multiplies
+                                  the sum by the RMS factor, so that it can start
+                                  per 128-column tile of x_out: the same map as
+                                  RMSNorm-then-QKV, with the bf16 rounding of the
+                                  normalised input moved                          */
 #define MK_TOPK_RENORM   0x4u  /* combine weights renormalised over the top-k    */
 #define MK_PREFETCH_NEXT_KV 0x8u /* in a stack (mk_stack_step), fetch the next
                                     layer's old KV rows -- those its verify tokens
