@@ -191,3 +191,56 @@ def test_moe_stack_62_layers(cuda_lib):
     work = synth.make_workload("moe_stack", device="cuda")
     assert [c["window"] for c in work["cfgs"]].count(0) == 16
     _check_stack(cuda_lib, work, subset={0, 1, 3, 30, 31, 59, 60, 61})
+
+
+def _run_stack(binding, work, extra_flags):
+    """One PDL-chained stack step on fresh copies of the caches; returns the
+    output, every layer's caches and router indices."""
+    cfgs, Ws = work["cfgs"], work["Ws"]
+    L = len(Ws)
+    T, ctx = work["wl"]["T"], work["wl"]["ctx"]
+    k = work["wl"].get("top_k", 1)
+    max_ctx = work["caches"][0][0].shape[0]
+    layers = []
+    try:
+        for l in range(L):
+            fuse = l + 1 < L
+            flags = (binding.MK_FIRST_LAYER if l == 0 else 0) | (binding.MK_FUSE_NEXT_QKV if fuse else 0)
+            if fuse:
+                flags |= extra_flags
+            layers.append(H.make_layer(binding, cfgs[l], Ws[l], flags, max_ctx,
+                                       next_W=Ws[l + 1] if fuse else None))
+        stack = binding.mk_stack_create(layers)
+        kcs = [c[0].clone() for c in work["caches"]]
+        vcs = [c[1].clone() for c in work["caches"]]
+        out = torch.zeros_like(work["x_in"][:T])
+        idx = torch.full((L, T, k), -1, dtype=torch.int32, device="cuda")
+        binding.mk_stack_step(stack, binding.make_stack_io(T, ctx, work["x_in"][:T].contiguous(), out,
+                                                           kcs, vcs, topk_idx_out=idx))
+        torch.cuda.synchronize()
+        st = binding.mk_stack_status(stack)
+        binding.mk_stack_destroy(stack)
+    finally:
+        for lay in layers:
+            binding.mk_layer_destroy(lay)
+    assert st == 0
+    return out, kcs, vcs, idx
+
+
+def test_next_layer_kv_prefetch_changes_no_output(cuda_lib):
+    """MK_PREFETCH_NEXT_KV only fetches the next layer's old K/V rows into L2:
+    a stack with it (4 tiny MoE layers, windows 32, global, 16, global, so both
+    kinds of visible range are fetched) gives the same output, caches and
+    router indices, bit for bit, as the stack without it."""
+    wl = dict(synth.WORKLOADS["tiny_layer"], layers=4, T=8, ctx=90)
+    work = synth.make_workload(wl, device="cpu")
+    for l, win in enumerate((32, 0, 16, 0)):
+        work["cfgs"][l] = dict(work["cfgs"][l], window=win)
+    for key in ("Ws", "caches", "x_in"):
+        work[key] = H.to_device(work[key], "cuda")
+    base = _run_stack(cuda_lib, work, 0)
+    pref = _run_stack(cuda_lib, work, cuda_lib.MK_PREFETCH_NEXT_KV)
+    assert torch.equal(base[0], pref[0])
+    for l in range(4):
+        assert torch.equal(base[1][l], pref[1][l]) and torch.equal(base[2][l], pref[2][l]), "layer %d" % l
+    assert torch.equal(base[3], pref[3])
